@@ -1,0 +1,377 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+* the E4M3 codec against PyTorch's independent float8_e4m3fn conversion (a library
+  routine the oracle does not use), plus round-trip / tie / saturation enumeration;
+* hand-derived worked examples under tests/golden/;
+* quantizers on inputs built by construction (codes and power-of-2 scales chosen
+  first, the BF16 input made from them), so the expected output is known without
+  evaluating the oracle's formula;
+* closed forms of the scale rule and the error bound of round-to-nearest;
+* the GEMM against a numpy matmul of dense dyadic matrices whose factorisation into
+  (codes, scales) the test builds itself, and against exact integer matmul.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def torch_decode(codes):
+    t = torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def torch_encode(vals):
+    t = torch.tensor(np.asarray(vals, np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def f32_bits_to_bf16_bits(h):
+    assert h & 0xFFFF == 0
+    return (h >> 16) & 0xFFFF
+
+
+def bf16_bits(x_f32: np.ndarray) -> np.ndarray:
+    """BF16 bits of float32 values that are exactly representable in BF16."""
+    b = np.asarray(x_f32, np.float32).view(np.uint32)
+    assert np.all(b & 0xFFFF == 0), "value not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+# ------------------------------------------------------------------ codec
+
+def test_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch_decode(codes)
+    nan_ours, nan_ref = np.isnan(ours), np.isnan(ref)
+    assert np.array_equal(nan_ours, nan_ref)
+    assert set(np.nonzero(nan_ours)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(ours[~nan_ours], ref[~nan_ref])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+    # signed zero
+    assert math.copysign(1.0, ours[0x80]) == -1.0
+
+
+def _probe_values():
+    rng = np.random.default_rng(7)
+    finite = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = (finite[:-1] + finite[1:]) / 2.0  # exact in float32
+    base = np.concatenate([finite, mids]).astype(np.float32)
+    ulp_up = np.nextafter(base, np.float32(np.inf))
+    ulp_dn = np.nextafter(base, np.float32(0))
+    rnd = np.concatenate([
+        rng.standard_normal(20000) * s for s in (1e-3, 1e-1, 1, 10, 100)
+    ]).astype(np.float32)
+    rnd = rnd[np.abs(rnd) <= 464]
+    tiny = np.array([1e-30, 1e-42, 2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11], np.float32)
+    v = np.concatenate([base, ulp_up, ulp_dn, rnd, tiny]).astype(np.float32)
+    v = np.concatenate([v, -v])
+    return v[np.abs(v) <= 464]
+
+
+def test_encode_matches_torch_in_range():
+    v = _probe_values()
+    assert np.array_equal(oracle.e4m3_encode(v), torch_encode(v))
+
+
+def test_encode_saturates():
+    big = np.array([448.0, 449.0, 464.0, 465.0, 1000.0, 3.0e38, np.inf], np.float32)
+    assert np.all(oracle.e4m3_encode(big) == 0x7E)
+    assert np.all(oracle.e4m3_encode(-big) == 0xFE)
+
+
+def test_round_trip_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = torch_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def test_midpoints_go_to_even_code():
+    codes = np.arange(0, 0x7E, dtype=np.uint8)
+    lo = torch_decode(codes)
+    hi = torch_decode(codes + 1)
+    mids = ((lo + hi) / 2).astype(np.float32)
+    expect = np.where(codes % 2 == 0, codes, codes + 1).astype(np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(mids), expect)
+    assert np.array_equal(oracle.e4m3_encode(-mids), expect | 0x80)
+
+
+# ---------------------------------------------------------- golden files
+
+def _read_tile_golden():
+    groups = {}
+    cur = None
+    with open(os.path.join(GOLDEN, "tile_1x128_worked.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "group":
+                cur = tok[1]
+                groups[cur] = {"amax": float(tok[2]), "scale": int(tok[3], 16), "elems": []}
+            else:
+                groups[cur]["elems"].append((int(tok[0]), int(tok[1], 16), int(tok[2], 16)))
+    return groups
+
+
+def test_golden_worked_tiles():
+    groups = _read_tile_golden()
+    assert set(groups) == {"A", "B", "C"}
+    x = np.zeros((len(groups), 128), np.uint16)
+    expect = np.zeros((len(groups), 128), np.uint8)
+    for r, name in enumerate(sorted(groups)):
+        for i, xbits, code in groups[name]["elems"]:
+            x[r, i] = f32_bits_to_bf16_bits(xbits)
+            expect[r, i] = code
+    q, s = oracle.quant_tile_1x128(x)
+    for r, name in enumerate(sorted(groups)):
+        assert s[0, r].view(np.uint32) == groups[name]["scale"], name
+    assert np.array_equal(q, expect)
+
+
+def test_golden_gemm_one_slice():
+    A = np.zeros((2, 128), np.uint8)
+    B = np.zeros((2, 128), np.uint8)
+    C = np.zeros((2, 2))
+    with open(os.path.join(GOLDEN, "gemm_k128_worked.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            t = line.split()
+            if t[0] == "A":
+                A[int(t[1]), int(t[2])] = int(t[3], 16)
+            elif t[0] == "B":
+                B[int(t[1]), int(t[2])] = int(t[3], 16)
+            elif t[0] == "SA":
+                sa = np.array([[float(t[1]), float(t[2])]], np.float32)
+            elif t[0] == "SB":
+                sb = np.array([[float(t[1])]], np.float32)
+            elif t[0] == "C":
+                C[int(t[1]), int(t[2])] = float(t[3])
+    ref, absref = oracle.gemm_ref(oracle.FPROP, A, sa, B, sb)
+    assert np.array_equal(ref, C)
+    assert absref[0, 0] == 2.5 and absref[1, 0] == 0.375
+
+
+# ------------------------------------------------------------ scale rule
+
+def test_scale_closed_forms():
+    assert oracle.group_scale(896.0) == np.float32(2.0)
+    assert oracle.group_scale(448.0) == np.float32(1.0)
+    assert oracle.group_scale(0.0) == np.float32(1.0)
+    assert oracle.group_scale(0.0, pow2=True) == np.float32(1.0)
+    assert oracle.group_scale(448.0, pow2=True) == np.float32(1.0)
+    assert oracle.group_scale(449.0, pow2=True) == np.float32(2.0)
+    assert oracle.group_scale(224.0, pow2=True) == np.float32(0.5)
+    assert oracle.group_scale(224.5, pow2=True) == np.float32(1.0)
+    # smallest BF16 subnormal: 2^-133 <= 448 * 2^e  <=>  e >= -141.8...  -> e = -141
+    assert oracle.group_scale(2.0 ** -133, pow2=True) == np.float32(2.0 ** -141)
+
+
+def test_pow2_scale_is_smallest_covering_power():
+    rng = np.random.default_rng(3)
+    amax = np.float32(np.exp(rng.uniform(-60, 60, 400))).astype(np.float32)
+    for a in amax:
+        s = float(oracle.group_scale(a, pow2=True))
+        e = math.frexp(s)[1] - 1
+        assert s == 2.0 ** e
+        assert float(a) <= 448.0 * 2.0 ** e
+        assert float(a) > 448.0 * 2.0 ** (e - 1)
+
+
+def test_amax_element_maps_to_448():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-20, 20, (64, 1)))).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    for pow2 in (False, True):
+        q, s = oracle.quant_tile_1x128(xb, pow2=pow2)
+        xf = (xb.astype(np.uint32) << 16).view(np.float32).reshape(64, 2, 128)
+        qq = q.reshape(64, 2, 128)
+        idx = np.abs(xf).argmax(axis=2)
+        top = np.take_along_axis(qq, idx[..., None], axis=2)[..., 0] & 0x7F
+        if not pow2:
+            assert np.all(top == 0x7E)
+        else:
+            # the largest magnitude lands in (224, 448]: codes 0x76 .. 0x7E
+            assert np.all((top >= 0x76) & (top <= 0x7E))
+
+
+# --------------------------------------------------- quantizers by construction
+
+def _constructed(rows, cols, grid_r, grid_c, rng, pow2_exps):
+    """Build a BF16 matrix from chosen codes and power-of-2 group scales.
+
+    Groups are grid_r x grid_c; in each group one element gets code 0x7E (448) so the
+    group's amax is exactly 448 * scale; the rest get random finite codes.  Returns
+    (x bf16 bits, codes, scales[gr, gc])."""
+    codes = rng.integers(0, 0x7F, size=(rows, cols)).astype(np.uint8)
+    codes |= (rng.integers(0, 2, size=(rows, cols)) * 0x80).astype(np.uint8)
+    gr, gc = rows // grid_r, cols // grid_c
+    exps = rng.choice(pow2_exps, size=(gr, gc))
+    for i in range(gr):
+        for j in range(gc):
+            r = i * grid_r + rng.integers(grid_r)
+            c = j * grid_c + rng.integers(grid_c)
+            codes[r, c] = 0x7E | (codes[r, c] & 0x80)
+    vals = torch_decode(codes)
+    sc = np.repeat(np.repeat(2.0 ** exps, grid_r, 0), grid_c, 1)
+    x = (vals * sc).astype(np.float32)
+    return bf16_bits(x), codes, (2.0 ** exps).astype(np.float32)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_tile_1x128_by_construction(pow2):
+    rng = np.random.default_rng(21)
+    xb, codes, sc = _constructed(40, 384, 1, 128, rng, np.arange(-20, 21))
+    q, s = oracle.quant_tile_1x128(xb, pow2=pow2)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(s, sc.T)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_tile_128x1_by_construction(pow2):
+    rng = np.random.default_rng(22)
+    xb, codes, sc = _constructed(256, 48, 128, 1, rng, np.arange(-20, 21))
+    qT, sT = oracle.quant_tile_128x1(xb, pow2=pow2)
+    assert np.array_equal(qT, codes.T)
+    assert np.array_equal(sT, sc)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_block_by_construction(pow2):
+    rng = np.random.default_rng(23)
+    xb, codes, sc = _constructed(256, 384, 128, 128, rng, np.arange(-20, 21))
+    q, qT, s = oracle.quant_block_128x128(xb, pow2=pow2, transposed=True)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(qT, codes.T)
+    assert np.array_equal(s, sc)
+
+
+def test_zero_groups():
+    x = np.zeros((3, 256), np.uint16)
+    x[1, :] = 0x8000  # -0.0
+    q, s = oracle.quant_tile_1x128(x)
+    assert np.all(s == 1.0)
+    assert np.all(q[0] == 0) and np.all(q[1] == 0x80) and np.all(q[2] == 0)
+
+
+def test_transposed_equals_row_quantizer_on_transpose():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((256, 384)) * rng.choice([1, 1, 50], size=(1, 384))).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    for pow2 in (False, True):
+        qT, sT = oracle.quant_tile_128x1(xb, pow2=pow2)
+        q2, s2 = oracle.quant_tile_1x128(np.ascontiguousarray(xb.T), pow2=pow2)
+        assert np.array_equal(qT, q2) and np.array_equal(sT, s2)
+
+
+def test_quantization_error_bound():
+    """Round-to-nearest: |dec(q) s - x| <= 2^-4 |x| where x/s is in the E4M3 normal
+    range (3 mantissa bits), and <= 2^-10 s below it (subnormal step 2^-9)."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((128, 512)) * np.exp(rng.uniform(-10, 10, (128, 1)))).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for pow2 in (False, True):
+        q, s = oracle.quant_tile_1x128(xb, pow2=pow2)
+        srow = np.repeat(s.T.astype(np.float64), 128, axis=1)
+        deq = torch_decode(q) * srow
+        err = np.abs(deq - xf)
+        y = np.abs(xf) / srow
+        normal = y >= 2.0 ** -6
+        slack = 1 + 2.0 ** -20  # the binary32 quotient's own rounding
+        assert np.all(err[normal] <= 2.0 ** -4 * np.abs(xf[normal]) * slack)
+        assert np.all(err[~normal] <= 2.0 ** -10 * srow[~normal] * slack)
+
+
+# ------------------------------------------------------------------ GEMM
+
+def _factor(dense, group_rows, group_cols, rng, exps=(-3, -2, -1, 0, 1, 2)):
+    """Factor a dense dyadic matrix into E4M3 codes and power-of-2 group scales chosen
+    by the test: codes = encode(dense / scale) exactly (values stay representable)."""
+    R, C = dense.shape
+    gr, gc = R // group_rows, C // group_cols
+    e = rng.choice(exps, size=(gr, gc))
+    sc = np.repeat(np.repeat(2.0 ** e, group_rows, 0), group_cols, 1)
+    codes = torch_encode((dense / sc).astype(np.float32))
+    assert np.array_equal(torch_decode(codes) * sc, dense)
+    return codes, (2.0 ** e).astype(np.float32)
+
+
+def _dyadic(rng, shape):
+    # small integers times a per-element power of two: exact through every step
+    return (rng.integers(-6, 7, size=shape) * 2.0 ** rng.integers(-2, 3, size=shape)).astype(np.float64)
+
+
+@pytest.mark.parametrize("op", ["fprop", "dgrad", "wgrad"])
+def test_gemm_matches_dense_dyadic_matmul(op):
+    rng = np.random.default_rng({"fprop": 1, "dgrad": 2, "wgrad": 3}[op])
+    M, N, K = 48, 256, 384
+    Ad = _dyadic(rng, (M, K))
+    Bd = _dyadic(rng, (N, K))
+    qa, sa = _factor(Ad, 1, 128, rng)            # 1x128 tiles: sa[m, kb]
+    sa_layout = np.ascontiguousarray(sa.T)       # [K/128, M]
+    if op == "fprop":
+        qb, sb = _factor(Bd, 128, 128, rng)      # blocks [N/128, K/128]
+        code, sb_layout = oracle.FPROP, sb
+    elif op == "dgrad":
+        qb, sb = _factor(Bd, 128, 128, rng)
+        code, sb_layout = oracle.DGRAD, np.ascontiguousarray(sb.T)  # [K/128, N/128]
+    else:
+        qb, sb = _factor(Bd, 1, 128, rng)        # per-row tiles sb[n, kb]
+        code, sb_layout = oracle.WGRAD, np.ascontiguousarray(sb.T)  # [K/128, N]
+    ref, absref = oracle.gemm_ref(code, qa, sa_layout, qb, sb_layout)
+    expect = Ad @ Bd.T
+    assert np.array_equal(ref, expect)
+    assert np.array_equal(absref, np.abs(Ad) @ np.abs(Bd).T)
+
+
+def test_gemm_small_integers_exact():
+    rng = np.random.default_rng(4)
+    vals = np.array([-4, -3, -2, -1, 0, 1, 2, 3, 4], np.float32)
+    M, N, K = 33, 128, 1024
+    ai = rng.choice(vals, size=(M, K)); bi = rng.choice(vals, size=(N, K))
+    qa, qb = torch_encode(ai), torch_encode(bi)
+    sa = np.ones((K // 128, M), np.float32)
+    sb = np.ones((1, K // 128), np.float32)
+    ref, _ = oracle.gemm_ref(oracle.FPROP, qa, sa, qb, sb)
+    assert np.array_equal(ref, (ai.astype(np.int64) @ bi.astype(np.int64).T).astype(np.float64))
+
+
+def test_gemm_ref_at_matches_full():
+    rng = np.random.default_rng(6)
+    qa = rng.integers(0, 0x7F, size=(20, 256)).astype(np.uint8)
+    qb = rng.integers(0, 0x7F, size=(128, 256)).astype(np.uint8)
+    sa = rng.uniform(0.1, 2, size=(2, 20)).astype(np.float32)
+    sb = rng.uniform(0.1, 2, size=(1, 2)).astype(np.float32)
+    full, fabs_ = oracle.gemm_ref(oracle.FPROP, qa, sa, qb, sb)
+    ms = rng.integers(0, 20, 50); ns = rng.integers(0, 128, 50)
+    at, aabs = oracle.gemm_ref_at(oracle.FPROP, qa, sa, qb, sb, ms, ns)
+    assert np.array_equal(at, full[ms, ns]) and np.array_equal(aabs, fabs_[ms, ns])
+
+
+def test_grouped_matches_per_expert_dense():
+    rng = np.random.default_rng(8)
+    G, N, K = 5, 128, 256
+    counts = np.array([3, 0, 130, 1, 0])
+    off = np.concatenate([[0], np.cumsum(counts)])
+    M = int(off[-1]) + 4  # 4 trailing rows belong to no expert
+    Ad = _dyadic(rng, (M, K))
+    qa, sa = _factor(Ad, 1, 128, rng)
+    Bd = [_dyadic(rng, (N, K)) for _ in range(G)]
+    fac = [_factor(b, 128, 128, rng) for b in Bd]
+    qb = np.stack([f[0] for f in fac]); sb = np.stack([f[1] for f in fac])
+    ref, _ = oracle.grouped_gemm_ref(off, qa, np.ascontiguousarray(sa.T), qb, sb)
+    expect = np.zeros((M, N))
+    for g in range(G):
+        expect[off[g]:off[g + 1]] = Ad[off[g]:off[g + 1]] @ Bd[g].T
+    assert np.array_equal(ref, expect)
