@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+One step = the dense Fprop of the pages' model width: 1x128 quantization of the BF16
+activations A [4096, 7168], 128x128 quantization of the BF16 weight W_lin [18432, 7168],
+and the block-scaled FP8 GEMM C = A W_lin^T (BF16 out), all in this library's kernels.
+
+Prints ONE JSON line (rank 0).  ``value`` is GEMM TFLOP/s of the whole step (the
+quantizers' time included) over all ranks; ``roofline`` describes the GEMM kernel
+against the dense FP8 tensor peak; ``rows`` times the other hot-path steps (fused dual
+quantizer, Dgrad, Wgrad, MoE prefill and decode grouped GEMMs) in the same run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20     # > 126 MB L2
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+FP8_PER_BF16 = 2.0             # nominal dense ratio fp8 : bf16 (4.5 : 2.25 PFLOP/s)
+M_DENSE, K_DENSE, N_DENSE = 4096, 7168, 18432
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def src_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["mixed_precision_quant_b300/csrc/gemm.cu", "mixed_precision_quant_b300/csrc/mpq_device.cuh"]
+
+
+def profiled_traffic(name: str, digest: str):
+    """DRAM bytes per launch recorded by an ncu capture summary under profiles/, if the
+    capture was taken of the current kernel source (matching digest); else None."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        kv = {}
+        with open(path) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_digest") != digest:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def cpu_oracle_sample(rows=256, feats=2048):
+    """Time the CPU oracle on a bounded sample of the dense Fprop workload: 1x128
+    quantization of ``rows`` activation rows, 128x128 quantization of ``feats`` weight
+    rows and the FP64 GEMM on those rows x feats outputs (K = 7168).
+    Returns (tflops_equivalent, seconds, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads
+
+    oracle.build()
+    g = torch.Generator().manual_seed(1)
+    a = workloads.normal((rows, K_DENSE), 1.0, g, "cpu")
+    w = workloads.normal((feats, K_DENSE), 0.02, g, "cpu")
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ab, wb = bits(a), bits(w)
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_tile_1x128(ab)
+    qb, _, sb = oracle.quant_block_128x128(wb)
+    oracle.gemm_ref(oracle.FPROP, qa, sa, qb, sb)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * feats * K_DENSE
+    desc = (f"oracle (single-threaded C): quantize {rows}x{K_DENSE} activations + {feats}x{K_DENSE} weight, "
+            f"FP64 GEMM on {rows}x{feats} outputs (K={K_DENSE}); rate = 2*{rows}*{feats}*{K_DENSE} / time")
+    return flops / dt / 1e12, dt, desc
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import mixed_precision_quant_b300 as mpq
+    import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    stream = torch.cuda.current_stream(dev)
+
+    d = workloads.dense_fprop(device=dev)
+    A, W = d["A"], d["W"]
+    M, K = A.shape
+    N = W.shape[0]
+    qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mpq.fp8_quant_tile_1x128(A, q=qa, s=sa)
+        mpq.fp8_quant_block_128x128(W, q=qb, s=sb)
+        mpq.fp8_gemm_blockscaled(mpq.FPROP, qa, sa, qb, sb, C=C)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, where = mpq.mpq_check_device_status(local_rank)
+    if st != 0:
+        raise RuntimeError(f"device status {st} at {where:#x} after warm-up")
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = [(ev(), ev(), ev(), ev()) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)        # L2 flush between timed steps (not timed)
+            e0, e1, e2, e3 = marks[i]
+            e0.record(stream)
+            mpq.fp8_quant_tile_1x128(A, q=qa, s=sa)
+            mpq.fp8_quant_block_128x128(W, q=qb, s=sb)
+            e1.record(stream)
+            mpq.fp8_gemm_blockscaled(mpq.FPROP, qa, sa, qb, sb, C=C)
+            e2.record(stream)
+            e3.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
+    gemm_ms = [m[1].elapsed_time(m[2]) for m in marks]
+    quant_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flop_step = 2.0 * M * N * K
+    value = flop_step * args.steps * world / (total_ms / 1e3) / 1e12
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    achieved = flop_step / (gemm_avg / 1e3) / 1e12
+    traffic = profiled_traffic("gemm_dense_fprop_4096x18432x7168.txt", src_digest(GEMM_SOURCES))
+    quant_bytes = M * K * (2 + 1 + 4 / 128) + N * K * 3 + (N // 128) * (K // 128) * 4
+
+    # end to end through the public API with host buffers: H2D inputs, D2H result per step
+    A_h = A.cpu().pin_memory()
+    W_h = W.cpu().pin_memory()
+    C_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    A_d = torch.empty_like(A)
+    W_d = torch.empty_like(W)
+    e2e_ms = []
+    for i in range(max(2, min(args.steps, 5)) + 1):
+        s0, s1 = ev(), ev()
+        s0.record(stream)
+        A_d.copy_(A_h, non_blocking=True)
+        W_d.copy_(W_h, non_blocking=True)
+        mpq.fp8_quant_tile_1x128(A_d, q=qa, s=sa)
+        mpq.fp8_quant_block_128x128(W_d, q=qb, s=sb)
+        mpq.fp8_gemm_blockscaled(mpq.FPROP, qa, sa, qb, sb, C=C)
+        C_h.copy_(C, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i > 0:  # first iteration is a warm-up of the copy path
+            e2e_ms.append(s0.elapsed_time(s1))
+    e2e_avg = sum(e2e_ms) / len(e2e_ms)
+    st, where = mpq.mpq_check_device_status(local_rank)
+    if st != 0:
+        raise RuntimeError(f"device status {st} at {where:#x}")
+
+    del d, A, W, qa, qb, C, A_d, W_d, flush
+    torch.cuda.empty_cache()
+    rows = {} if args.no_rows else measure_rows(mpq, workloads, dev, peaks, fp8_peak)
+
+    result = {
+        "metric": "block-scaled FP8 GEMM TFLOP/s (% of B300 FP8 peak); quantizer GB/s (% of HBM)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded; shapes of the pages' model)",
+        "config": {"workload": "dense Fprop step: 1x128 quant A[4096,7168] + 128x128 quant W[18432,7168] "
+                               "+ block-scaled FP8 GEMM 4096x18432x7168, BF16 out",
+                   "M": M, "N": N, "K": K, "l2": "flushed between timed steps (256 MB write, untimed)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (block-scaled FP8, 128-K promotion)",
+                     "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                     "peak_note": f"FP8 dense = {FP8_PER_BF16:g} x {peaks['source']} bf16 burst "
+                                  f"{peaks['bf16_tflops']} TFLOP/s (nominal fp8:bf16 ratio)",
+                     "gemm_ms": round(gemm_avg, 4)},
+        "step_breakdown_ms": {"quantizers": round(sum(quant_ms) / len(quant_ms), 4),
+                              "gemm": round(gemm_avg, 4),
+                              "quantizers_GBps": round(quant_bytes / (sum(quant_ms) / len(quant_ms) / 1e3) / 1e9, 1)},
+        "e2e": {"value": round(flop_step / (e2e_avg / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_avg, 3),
+                "h2d_bytes_per_step": int(M * K * 2 + N * K * 2), "d2h_bytes_per_step": int(M * N * 2)},
+        "clocks": clk.summary(),
+        "rows": rows,
+    }
+    return result
+
+
+def timed(fn, flush, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        a.record(); fn(); b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sum(ts) / len(ts)
+
+
+def measure_rows(mpq, workloads, dev, peaks, fp8_peak):
+    """Time every other hot-path step on its configuration (CUDA events, L2 flushed)."""
+    import torch
+    hbm = peaks["hbm_gbs"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+
+    def gb(nbytes, ms):
+        return nbytes / (ms / 1e3) / 1e9
+
+    # ---- backward pair: fused dual quantizer (X), pow2 dual quantizer (dY), Dgrad, Wgrad
+    d = workloads.backward_pair(device=dev)
+    dY, X, Wl = d["dY"], d["X"], d["W"]
+    T, Nout = dY.shape
+    Kin = X.shape[1]
+    qx, sx, qxT, sxT = mpq.fp8_quant_tile_1x128(X, transposed=True)
+    ms = timed(lambda: mpq.fp8_quant_tile_1x128(X, q=qx, s=sx, qT=qxT, sT=sxT, transposed=True), flush)
+    nbytes = T * Kin * (2 + 2 + 8 / 128)
+    out["dual_quant_X_8192x7168"] = {"ms": round(ms, 4), "GBps": round(gb(nbytes, ms), 1),
+                                     "frac_hbm": round(gb(nbytes, ms) / hbm, 4), "bound": "hbm"}
+    qdy, sdy, qdyT, sdyT = mpq.fp8_quant_tile_1x128(dY, pow2=True, transposed=True)
+    ms = timed(lambda: mpq.fp8_quant_tile_1x128(dY, pow2=True, q=qdy, s=sdy, qT=qdyT, sT=sdyT, transposed=True), flush)
+    nbytes = T * Nout * (2 + 2 + 8 / 128)
+    out["dual_quant_pow2_dY_8192x2048"] = {"ms": round(ms, 4), "GBps": round(gb(nbytes, ms), 1),
+                                           "frac_hbm": round(gb(nbytes, ms) / hbm, 4), "bound": "hbm"}
+    qw, qwT, sw = mpq.fp8_quant_block_128x128(Wl, transposed=True)
+    ms = timed(lambda: mpq.fp8_quant_block_128x128(Wl, q=qw, qT=qwT, s=sw, transposed=True), flush)
+    nbytes = Nout * Kin * 4
+    out["block_quant_transposed_W_2048x7168"] = {"ms": round(ms, 4), "GBps": round(gb(nbytes, ms), 1),
+                                                 "frac_hbm": round(gb(nbytes, ms) / hbm, 4), "bound": "hbm"}
+    dX = torch.empty((T, Kin), dtype=torch.float32, device=dev)
+    ms = timed(lambda: mpq.fp8_gemm_blockscaled(mpq.DGRAD, qdy, sdy, qwT, sw, out_dtype=mpq.OUT_FP32, C=dX), flush)
+    fl = 2.0 * T * Kin * Nout
+    out["dgrad_8192x7168x2048_fp32"] = {"ms": round(ms, 4), "TFLOPs": round(fl / ms / 1e9, 1),
+                                        "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4), "bound": "tensor"}
+    dW = torch.empty((Kin, Nout), dtype=torch.float32, device=dev)
+    ms = timed(lambda: mpq.fp8_gemm_blockscaled(mpq.WGRAD, qxT, sxT, qdyT, sdyT, out_dtype=mpq.OUT_FP32, C=dW), flush)
+    out["wgrad_7168x2048x8192_fp32"] = {"ms": round(ms, 4), "TFLOPs": round(fl / ms / 1e9, 1),
+                                        "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4), "bound": "tensor"}
+    del d, dY, X, Wl, qx, sx, qxT, sxT, qdy, sdy, qdyT, sdyT, qw, qwT, sw, dX, dW
+    torch.cuda.empty_cache()
+
+    # ---- MoE prefill and decode: 1x128 activation quantization + grouped GEMM, up and down
+    for name, gen in (("moe_prefill", workloads.moe_prefill), ("moe_decode", workloads.moe_decode)):
+        d = gen(device=dev)
+        off = d["offsets"].to(dev)
+        res = {"tokens_routed": int(d["offsets"][-1]),
+               "experts_nonempty": int((d["counts"] > 0).sum())}
+        total_ms, total_flops, w_bytes = 0.0, 0.0, 0
+        for proj, pow2 in (("up", False), ("down", True)):
+            X = d["X_up"] if proj == "up" else d["X_dn"]
+            Wt = d["W_up"] if proj == "up" else d["W_dn"]
+            G, N, K = Wt.shape
+            qw = torch.empty((G, N, K), dtype=torch.uint8, device=dev)
+            sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=dev)
+            for e in range(G):
+                mpq.fp8_quant_block_128x128(Wt[e], q=qw[e], s=sw[e])
+            del Wt
+            if proj == "up":
+                del d["W_up"]
+            else:
+                del d["W_dn"]
+            torch.cuda.empty_cache()
+            qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X, pow2=pow2)
+            C = torch.empty((X.shape[0], N), dtype=torch.bfloat16, device=dev)
+
+            def run():
+                mpq.fp8_quant_tile_1x128(X, pow2=pow2, q=qx, s=sx)
+                mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qw, sw, C=C)
+
+            ms = timed(run, flush)
+            fl = 2.0 * X.shape[0] * N * K
+            wb = G * N * K + G * (N // 128) * (K // 128) * 4
+            res[proj] = {"ms": round(ms, 4), "TFLOPs": round(fl / ms / 1e9, 1),
+                         "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4),
+                         "weight_GBps": round(gb(wb, ms), 1), "frac_hbm_weights": round(gb(wb, ms) / hbm, 4)}
+            total_ms += ms
+            total_flops += fl
+            w_bytes += wb
+            del qw, sw, qx, sx, C
+            torch.cuda.empty_cache()
+        res["total_ms"] = round(total_ms, 4)
+        res["TFLOPs"] = round(total_flops / total_ms / 1e9, 1)
+        res["frac_fp8_peak"] = round(total_flops / total_ms / 1e9 / fp8_peak, 4)
+        res["weight_bytes"] = w_bytes
+        res["frac_hbm_weights"] = round(gb(w_bytes, total_ms) / hbm, 4)
+        res["bound"] = "tensor" if name == "moe_prefill" else "hbm"
+        out[name] = res
+        del d
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the bounded dense-Fprop sample."""
+    # each step ~2 s of single-core work so that --steps 20 --warmup 3 ends in ~1 minute
+    for _ in range(args.warmup):
+        cpu_oracle_sample(64, 512)
+    vals, secs = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        v, dt, desc = cpu_oracle_sample(128, 1024)
+        vals.append(v)
+        secs += dt
+    value = sum(vals) / len(vals)
+    return {
+        "impl": "reference",
+        "metric": "block-scaled FP8 GEMM TFLOP/s (% of B300 FP8 peak); quantizer GB/s (% of HBM)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp64 oracle on fp8 e4m3 codes", "data": "synthetic",
+        "config": {"workload": "dense Fprop step (bounded sample): 1x128 quant A + 128x128 quant W + GEMM, "
+                               "M=4096 N=18432 K=7168", "M": M_DENSE, "N": N_DENSE, "K": K_DENSE},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu:
+            v, dt, desc = cpu_oracle_sample()
+            res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc,
+                                   "seconds": round(dt, 2)}
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

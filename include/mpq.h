@@ -1,0 +1,201 @@
+/*
+ * mpq.h -- C ABI of libmpq: fine-grained FP8 (E4M3) quantization and block-scaled
+ * FP8 GEMM for NVIDIA B300 (sm_103a), one GPU, one process.
+ *
+ * The method is the fine-grained FP8 mixed-precision scheme of an MoE transformer's
+ * training framework as described by the source pages (scraped copies of its technical
+ * report):
+ *   - page 1 (second paragraph): the scaling factor is derived from the online max-abs
+ *     value and activations or weights are quantized online into FP8; the FP8 GEMMs
+ *     accept FP8 tensors and produce BF16 or FP32 outputs; activations are cached in FP8
+ *     for the backward pass;
+ *   - page 2, "9 Amazing Deepseek Hacks" (last paragraph): groups of 128 activation
+ *     values; in the backward pass the matrix is read, transposed and re-quantized into
+ *     128x1 tiles;
+ *   - page 3 (first paragraph): the max-abs value is scaled to the largest FP8 value;
+ *   - page 4 (first paragraph): partial sums are promoted every 128 elements of K and
+ *     accumulated in full FP32; (second paragraph): Fprop, Dgrad and Wgrad all run in
+ *     FP8, with integral power-of-2 scaling factors for some activations;
+ *   - page 4 (third paragraph): during decoding the batch per expert is small (usually
+ *     within 256 tokens) and the expert GEMM is bound by memory access.
+ * E4M3 is the OCP FP8 format (bias 7, no infinities, largest finite value 448).
+ *
+ * Conventions for every call
+ *   - Every pointer except the handle is a DEVICE pointer owned by the caller; the
+ *     library never frees or retains it after the call returns.
+ *   - Matrices are row-major; ld* is the row stride in ELEMENTS of that array.
+ *   - BF16 inputs are passed as `const void *` (16-bit bfloat16 elements).
+ *   - E4M3 codes are bytes; scales are float32.
+ *   - `stream` is a cudaStream_t (passed as void *); every call only enqueues work on
+ *     it and returns without synchronizing.  The caller's device must be current.
+ *   - Arguments are validated on the host before anything is launched; a validation
+ *     failure returns a status code and leaves all outputs untouched.
+ *   - Device-side waits are bounded (about one second by default).  A wait that runs
+ *     out records MPQ_ERR_TIMEOUT in the handle's device status word and the kernel
+ *     exits cleanly; mpq_check_device_status() reports it.
+ */
+#ifndef MPQ_H
+#define MPQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mpq_status {
+    MPQ_OK = 0,
+    MPQ_ERR_NULL = 1,        /* a required pointer is NULL                                */
+    MPQ_ERR_SHAPE = 2,       /* a size or leading dimension is invalid                    */
+    MPQ_ERR_ALIGN = 3,       /* a pointer or stride breaks the 16-byte (or 4-byte) rule    */
+    MPQ_ERR_UNSUPPORTED = 4, /* unknown op, dtype or flag combination                     */
+    MPQ_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed                       */
+    MPQ_ERR_TIMEOUT = 6      /* a device-side wait ran out (reported by the status word)  */
+} mpq_status;
+
+typedef enum mpq_op {
+    MPQ_OP_FPROP = 0, /* sB: 128x128 weight blocks, layout [N/128][ldsb >= K/128]        */
+    MPQ_OP_DGRAD = 1, /* sB: 128x128 weight blocks seen through the transposed weight,
+                         layout [K/128][ldsb >= N/128]                                   */
+    MPQ_OP_WGRAD = 2  /* sB: 128x1 token tiles of B, layout [K/128][ldsb >= N]           */
+} mpq_op;
+
+typedef enum mpq_dtype {
+    MPQ_OUT_BF16 = 0,
+    MPQ_OUT_FP32 = 1
+} mpq_dtype;
+
+/* Flags */
+#define MPQ_POW2 1u /* power-of-2 scales: s = 2^e, e the smallest integer with amax <= 448*2^e */
+
+typedef struct mpq_handle_s *mpq_handle;
+
+/* Library version string, e.g. "mpq 0.1.0 sm_103a". */
+const char *mpq_version(void);
+
+/* Human-readable text of a status code (static storage). */
+const char *mpq_status_string(int status);
+
+/* Create a handle bound to the current CUDA device.  Allocates the 8-byte device
+ * status word (cudaMalloc) and caches the SM count.  Not thread-safe per handle. */
+mpq_status mpq_create(mpq_handle *out);
+
+/* Destroy a handle and free its status word.  Synchronizes the device first. */
+mpq_status mpq_destroy(mpq_handle h);
+
+/* Limit for every device-side wait launched through this handle, in nanoseconds
+ * (default 1e9).  0 restores the default. */
+mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
+
+/* Synchronize `stream`, read and clear the device status word.  Returns MPQ_OK or the
+ * recorded error (MPQ_ERR_TIMEOUT); *where_out (may be NULL) receives the tag of the
+ * wait that gave up (role << 8 | barrier index), 0 if none. */
+mpq_status mpq_check_device_status(mpq_handle h, void *stream, int *where_out);
+
+/*
+ * fp8_quant_tile_1x128 -- activation quantization in 1x128 tiles (page 1, second
+ * paragraph; page 2, last paragraph; page 3, first paragraph), with an optional fused
+ * 128x1 (along-rows) quantization written transposed for the Wgrad operand (page 2,
+ * last paragraph: re-quantized into 128x1 tiles).
+ *
+ *   x    [rows, cols] BF16, ldx >= cols.
+ *   Row-wise output (skipped when q == NULL; then s is ignored):
+ *        q [rows, cols] E4M3, ldq >= cols;
+ *        s [cols/128][lds] float32, lds >= rows: s[kb*lds + r] is the scale of
+ *          x[r, kb*128 .. kb*128+127].
+ *   Transposed output (only when qT != NULL):
+ *        qT [cols, rows] E4M3, ldqT >= rows: qT[c, r] is the code of x[r, c] within the
+ *          group x[rb*128 .. rb*128+127, c], rb = r/128;
+ *        sT [rows/128][ldsT] float32, ldsT >= cols: sT[rb*ldsT + c].
+ *   flags: 0 or MPQ_POW2.
+ * Each group: amax = max |x|; s = amax/448 as one binary32 division (1.0 when amax is 0)
+ * or the power of 2 above; code = E4M3 round-to-nearest-even of the binary32 quotient
+ * x/s, saturating at +-448; zero keeps its sign.
+ * Requirements: cols % 128 == 0; rows % 128 == 0 when qT != NULL; rows >= 0.
+ * x, q, qT 16-byte aligned; ldx % 8 == 0; ldq and ldqT % 16 == 0; s, sT 4-byte aligned.
+ * At least one of q, qT must be non-NULL.
+ */
+mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                uint8_t *qT, int64_t ldqT, float *sT, int64_t ldsT,
+                                uint32_t flags, void *stream);
+
+/*
+ * fp8_quant_block_128x128 -- weight quantization in 128x128 blocks (page 1, second
+ * paragraph: weights are quantized online from their max-abs value), optionally also
+ * writing the transposed codes (same scales) used as the Dgrad B operand.
+ *
+ *   w  [rows, cols] BF16, ldw >= cols;
+ *   q  [rows, cols] E4M3, ldq >= cols;
+ *   qT [cols, rows] E4M3 or NULL, ldqT >= rows: qT[c, r] == q[r, c];
+ *   s  [rows/128][lds] float32, lds >= cols/128: s[i*lds + j] scales block (i, j).
+ *   flags: 0 or MPQ_POW2.
+ * Requirements: rows % 128 == 0, cols % 128 == 0; w, q, qT 16-byte aligned; ldw % 8 == 0;
+ * ldq, ldqT % 16 == 0; s 4-byte aligned.
+ */
+mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, int64_t cols, int64_t ldw,
+                                   uint8_t *q, int64_t ldq, uint8_t *qT, int64_t ldqT,
+                                   float *s, int64_t lds, uint32_t flags, void *stream);
+
+/*
+ * fp8_gemm_blockscaled -- block-scaled FP8 GEMM with 128-element FP32 promotion
+ * (page 4, first paragraph; page 1, second paragraph; page 4, second paragraph: Fprop,
+ * Dgrad and Wgrad in FP8):
+ *
+ *   C[m, n] = sum_kb ( sum_{k = 128 kb}^{128 kb + 127} A[m,k] B[n,k] ) * sA[kb*ldsa + m] * sB(n, kb)
+ *
+ *   A  [M, K] E4M3, lda >= K (K-major);   sA [K/128][ldsa] float32, ldsa >= M.
+ *   B  [N, K] E4M3, ldb >= K (K-major);   sB per `op`:
+ *        MPQ_OP_FPROP  sB[(n/128)*ldsb + kb]  (weight blocks; B = the quantized weight)
+ *        MPQ_OP_DGRAD  sB[kb*ldsb + n/128]    (weight blocks of the weight whose
+ *                                              transposed codes are B)
+ *        MPQ_OP_WGRAD  sB[kb*ldsb + n]        (128x1 token tiles written transposed)
+ *   C  [M, N] BF16 (out = MPQ_OUT_BF16, round to nearest even) or FP32, ldc >= N.
+ * Within a 128-K slice the products are summed by the tensor cores in FP32; each slice
+ * is then scaled and added into an FP32 accumulator.
+ * Requirements: M >= 0, N % 128 == 0, K % 128 == 0, K > 0; A, B, C 16-byte aligned;
+ * lda, ldb % 16 == 0; ldc * sizeof(out) % 16 == 0; sA, sB 4-byte aligned.
+ */
+mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int64_t K,
+                                const uint8_t *A, int64_t lda, const float *sA, int64_t ldsa,
+                                const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                void *C, int64_t ldc, int out_dtype, void *stream);
+
+/*
+ * fp8_grouped_gemm_blockscaled -- MoE expert GEMMs (page 2, first paragraph: large
+ * per-expert batches in training; page 4, third paragraph: small per-expert batches in
+ * decoding), Fprop scaling per expert:
+ *
+ *   for g in [0, G): rows [off[g], off[g+1]) of A and C use weight B_g:
+ *   C[m, n] = sum_kb (sum_k A[m,k] B_g[n,k]) * sA[kb*ldsa + m] * sB_g[(n/128)*ldsb + kb]
+ *
+ *   d_offsets  DEVICE int64 [G+1], non-decreasing, 0 <= off[g] <= M_total (the kernel
+ *              clamps into this range; rows outside every expert are not written).
+ *   A          [M_total, K] E4M3, lda >= K;  sA [K/128][ldsa] float32, ldsa >= M_total.
+ *   B          [G][N][K] E4M3 (expert g at B + g*N*ldb), ldb >= K.
+ *   sB         [G][N/128][ldsb] float32 (expert g at sB + g*(N/128)*ldsb), ldsb >= K/128.
+ *   C          [M_total, N] BF16 or FP32, ldc >= N.
+ *   flags      0 (reserved).
+ * Requirements: 1 <= G <= 1024; N % 128 == 0; K % 128 == 0; alignment as for
+ * fp8_gemm_blockscaled.
+ */
+mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets,
+                                        int64_t M_total, int64_t N, int64_t K,
+                                        const uint8_t *A, int64_t lda, const float *sA, int64_t ldsa,
+                                        const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                        void *C, int64_t ldc, int out_dtype, uint32_t flags,
+                                        void *stream);
+
+/*
+ * mpq_selftest_wait_timeout -- launches one CTA that waits on a barrier nothing ever
+ * arrives on, with the library's bounded wait and the given limit (nanoseconds).  The
+ * wait must give up and record MPQ_ERR_TIMEOUT in the handle's status word; the
+ * context stays usable.  Used to test device-side failure reporting without a fault.
+ */
+mpq_status mpq_selftest_wait_timeout(mpq_handle h, uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPQ_H */

@@ -1,0 +1,240 @@
+"""mixed_precision_quant_b300 -- Python binding of libmpq (fine-grained FP8 quantization
+and block-scaled FP8 GEMM on B300 / sm_103a).
+
+This module only marshals arguments: it turns torch tensors into device pointers,
+leading dimensions and the current CUDA stream, calls the C ABI declared in
+``include/mpq.h`` (same function names), and raises :class:`MPQError` on a non-zero
+status.  PyTorch is used for device memory and streams only; every step of the path
+runs in the library's own CUDA kernels.  There is no fallback: if ``libmpq.so`` is
+missing or cannot be loaded, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmpq.so")
+
+FPROP, DGRAD, WGRAD = 0, 1, 2
+OUT_BF16, OUT_FP32 = 0, 1
+POW2 = 1
+
+_STATUS = {0: "ok", 1: "null pointer argument", 2: "invalid size or leading dimension",
+           3: "misaligned pointer or stride", 4: "unsupported op, dtype or flags",
+           5: "CUDA call failed", 6: "device-side wait timed out"}
+
+
+class MPQError(RuntimeError):
+    def __init__(self, fn: str, status: int, extra: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)}{extra}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libmpq.so is not built ({LIB_PATH}); run `python -m mixed_precision_quant_b300._build` "
+            "or __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, U32, U64, INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int
+    sigs = {
+        "mpq_version": (ctypes.c_char_p, []),
+        "mpq_status_string": (ctypes.c_char_p, [INT]),
+        "mpq_create": (INT, [ctypes.POINTER(P)]),
+        "mpq_destroy": (INT, [P]),
+        "mpq_set_wait_timeout": (INT, [P, U64]),
+        "mpq_check_device_status": (INT, [P, P, ctypes.POINTER(INT)]),
+        "fp8_quant_tile_1x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, P, I, U32, P]),
+        "fp8_quant_block_128x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
+        "fp8_gemm_blockscaled": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
+        "fp8_grouped_gemm_blockscaled": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, U32, P]),
+        "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+_handles: dict = {}
+_hlock = threading.Lock()
+
+
+def version() -> str:
+    return _lib.mpq_version().decode()
+
+
+def _handle(device: torch.device) -> ctypes.c_void_p:
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    with _hlock:
+        h = _handles.get(idx)
+        if h is None:
+            with torch.cuda.device(idx):
+                h = ctypes.c_void_p()
+                st = _lib.mpq_create(ctypes.byref(h))
+                if st != 0:
+                    raise MPQError("mpq_create", st)
+            _handles[idx] = h
+        return h
+
+
+def _stream(device: torch.device, stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _ld(t: Optional[torch.Tensor]) -> int:
+    if t is None:
+        return 0
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise MPQError(fn, st)
+
+
+def _cuda2d(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or t.dim() != 2:
+        raise TypeError(f"{name}: expected a 2-D {dtype} CUDA tensor, got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+# ------------------------------------------------------------------- quantizers
+
+def fp8_quant_tile_1x128(x: torch.Tensor, *, pow2: bool = False, rows_out: bool = True,
+                         transposed: bool = False, q=None, s=None, qT=None, sT=None, stream=None):
+    """1x128 activation quantization of BF16 ``x [rows, cols]``.
+
+    Returns ``(q, s, qT, sT)``: row-wise codes ``q [rows, cols]`` uint8 with scales
+    ``s [cols/128, rows]`` float32 (None when ``rows_out`` is False), and, when
+    ``transposed``, the 128x1 (along rows) quantization stored transposed:
+    ``qT [cols, rows]`` with ``sT [rows/128, cols]``."""
+    _cuda2d(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    dev = x.device
+    if rows_out:
+        q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        s = s if s is not None else torch.empty((cols // 128, rows), dtype=torch.float32, device=dev)
+    else:
+        q = s = None
+    if transposed:
+        qT = qT if qT is not None else torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        sT = sT if sT is not None else torch.empty((rows // 128, cols), dtype=torch.float32, device=dev)
+    else:
+        qT = sT = None
+    st = _lib.fp8_quant_tile_1x128(_handle(dev), _ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q), _ptr(s), _ld(s),
+                                   _ptr(qT), _ld(qT), _ptr(sT), _ld(sT), POW2 if pow2 else 0,
+                                   _stream(dev, stream))
+    _check("fp8_quant_tile_1x128", st)
+    return q, s, qT, sT
+
+
+def fp8_quant_block_128x128(w: torch.Tensor, *, pow2: bool = False, transposed: bool = False,
+                            q=None, qT=None, s=None, stream=None):
+    """128x128 block quantization of BF16 ``w [rows, cols]``.
+
+    Returns ``(q [rows, cols], qT [cols, rows] or None, s [rows/128, cols/128])``."""
+    _cuda2d(w, torch.bfloat16, "w")
+    rows, cols = w.shape
+    dev = w.device
+    q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if transposed:
+        qT = qT if qT is not None else torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    else:
+        qT = None
+    s = s if s is not None else torch.empty((rows // 128, cols // 128), dtype=torch.float32, device=dev)
+    st = _lib.fp8_quant_block_128x128(_handle(dev), _ptr(w), rows, cols, _ld(w), _ptr(q), _ld(q), _ptr(qT),
+                                      _ld(qT), _ptr(s), _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
+    _check("fp8_quant_block_128x128", st)
+    return q, qT, s
+
+
+# ------------------------------------------------------------------------ GEMMs
+
+def _out(M, N, out_dtype, C, dev):
+    if C is not None:
+        return C
+    dt = torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16
+    return torch.empty((M, N), dtype=dt, device=dev)
+
+
+def fp8_gemm_blockscaled(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor, *,
+                         out_dtype: int = OUT_BF16, C: Optional[torch.Tensor] = None, stream=None):
+    """Block-scaled FP8 GEMM ``C[M, N] = sum_kb (A_kb B_kb^T) sA sB`` (see mpq.h).
+
+    ``A [M, K]`` and ``B [N, K]`` uint8 E4M3 codes, ``sA [K/128, M]`` float32, ``sB`` per op:
+    FPROP ``[N/128, K/128]``, DGRAD ``[K/128, N/128]``, WGRAD ``[K/128, N]``."""
+    _cuda2d(A, torch.uint8, "A"); _cuda2d(B, torch.uint8, "B")
+    _cuda2d(sA, torch.float32, "sA"); _cuda2d(sB, torch.float32, "sB")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    dev = A.device
+    C = _out(M, N, out_dtype, C, dev)
+    st = _lib.fp8_gemm_blockscaled(_handle(dev), int(op), M, N, K, _ptr(A), _ld(A), _ptr(sA), _ld(sA), _ptr(B),
+                                   _ld(B), _ptr(sB), _ld(sB), _ptr(C), _ld(C), int(out_dtype),
+                                   _stream(dev, stream))
+    _check("fp8_gemm_blockscaled", st)
+    return C
+
+
+def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,
+                                 sB: torch.Tensor, *, out_dtype: int = OUT_BF16, C: Optional[torch.Tensor] = None,
+                                 stream=None):
+    """MoE grouped FP8 GEMM: rows ``[off[g], off[g+1])`` of ``A`` use expert ``g``'s weight.
+
+    ``offsets`` int64 CUDA ``[G+1]``; ``A [M, K]`` codes, ``sA [K/128, M]``; ``B [G, N, K]`` codes;
+    ``sB [G, N/128, K/128]``.  Rows outside every expert are left untouched in ``C``."""
+    _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
+    if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.dim() == 1 and offsets.is_contiguous()):
+        raise TypeError("offsets: expected a contiguous 1-D int64 CUDA tensor")
+    if not (B.is_cuda and B.dtype == torch.uint8 and B.dim() == 3 and B.is_contiguous()):
+        raise TypeError("B: expected a contiguous [G, N, K] uint8 CUDA tensor")
+    if not (sB.is_cuda and sB.dtype == torch.float32 and sB.dim() == 3 and sB.is_contiguous()):
+        raise TypeError("sB: expected a contiguous [G, N/128, K/128] float32 CUDA tensor")
+    G, N, K = B.shape
+    M = A.shape[0]
+    if offsets.numel() != G + 1 or A.shape[1] != K:
+        raise ValueError("shape mismatch between offsets, A and B")
+    dev = A.device
+    C = _out(M, N, out_dtype, C, dev)
+    st = _lib.fp8_grouped_gemm_blockscaled(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(A), _ld(A), _ptr(sA),
+                                           _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
+                                           int(out_dtype), 0, _stream(dev, stream))
+    _check("fp8_grouped_gemm_blockscaled", st)
+    return C
+
+
+# --------------------------------------------------------------------- status
+
+def mpq_check_device_status(device=None, stream=None):
+    """Synchronize the stream and return (status, where) from the device status word."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    where = ctypes.c_int(0)
+    st = _lib.mpq_check_device_status(_handle(dev), _stream(dev, stream), ctypes.byref(where))
+    return st, where.value
+
+
+def mpq_set_wait_timeout(timeout_ns: int, device=None):
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    _check("mpq_set_wait_timeout", _lib.mpq_set_wait_timeout(_handle(dev), int(timeout_ns)))
+
+
+def mpq_selftest_wait_timeout(timeout_ns: int = 1_000_000, device=None, stream=None):
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    _check("mpq_selftest_wait_timeout", _lib.mpq_selftest_wait_timeout(_handle(dev), int(timeout_ns),
+                                                                         _stream(dev, stream)))

@@ -1,0 +1,294 @@
+// api.cu -- the C ABI of libmpq: handle, host-side validation, TMA descriptor
+// encoding and launches.  See include/mpq.h for the contract of every entry point.
+#include "mpq.h"
+#include "mpq_internal.h"
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+struct mpq_handle_s {
+    int device;
+    int num_sms;
+    int *d_status;          // [0] code, [1] tag of the wait that gave up
+    uint64_t timeout_ns;
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 2-D E4M3 operand view [rows, cols] (cols contiguous), box 128 (cols) x box_rows,
+// 128-byte swizzle, out-of-bounds rows read as zero.
+mpq_status encode_operand(CUtensorMap *m, const uint8_t *ptr, int64_t rows, int64_t cols, int64_t ld,
+                          uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return MPQ_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
+}
+
+mpq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPQ_OK : MPQ_ERR_CUDA; }
+
+} // namespace
+
+extern "C" {
+
+const char *mpq_version(void) { return "mpq 0.1.0 sm_103a"; }
+
+const char *mpq_status_string(int s)
+{
+    switch (s) {
+    case MPQ_OK: return "ok";
+    case MPQ_ERR_NULL: return "null pointer argument";
+    case MPQ_ERR_SHAPE: return "invalid size or leading dimension";
+    case MPQ_ERR_ALIGN: return "misaligned pointer or stride";
+    case MPQ_ERR_UNSUPPORTED: return "unsupported op, dtype or flags";
+    case MPQ_ERR_CUDA: return "CUDA call failed";
+    case MPQ_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+mpq_status mpq_create(mpq_handle *out)
+{
+    if (out == nullptr)
+        return MPQ_ERR_NULL;
+    *out = nullptr;
+    mpq_handle h = new (std::nothrow) mpq_handle_s();
+    if (h == nullptr)
+        return MPQ_ERR_CUDA;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&h->d_status), 2 * sizeof(int)) != cudaSuccess) {
+        delete h;
+        return MPQ_ERR_CUDA;
+    }
+    if (cudaMemset(h->d_status, 0, 2 * sizeof(int)) != cudaSuccess) {
+        cudaFree(h->d_status);
+        delete h;
+        return MPQ_ERR_CUDA;
+    }
+    h->timeout_ns = kDefaultTimeoutNs;
+    *out = h;
+    return MPQ_OK;
+}
+
+mpq_status mpq_destroy(mpq_handle h)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    cudaDeviceSynchronize();
+    cudaError_t e = cudaFree(h->d_status);
+    delete h;
+    return from_cuda(e);
+}
+
+mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    h->timeout_ns = timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns;
+    return MPQ_OK;
+}
+
+mpq_status mpq_check_device_status(mpq_handle h, void *stream, int *where_out)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int hs[2] = {0, 0};
+    if (cudaStreamSynchronize(st) != cudaSuccess ||
+        cudaMemcpy(hs, h->d_status, sizeof(hs), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->d_status, 0, sizeof(hs)) != cudaSuccess)
+        return MPQ_ERR_CUDA;
+    if (where_out != nullptr)
+        *where_out = hs[1];
+    return hs[0] == 0 ? MPQ_OK : static_cast<mpq_status>(hs[0]);
+}
+
+mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t *q, int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
+                                float *sT, int64_t ldsT, uint32_t flags, void *stream)
+{
+    if (h == nullptr || x == nullptr || (q == nullptr && qT == nullptr))
+        return MPQ_ERR_NULL;
+    if ((q != nullptr && s == nullptr) || (qT != nullptr && sT == nullptr))
+        return MPQ_ERR_NULL;
+    if (flags & ~MPQ_POW2)
+        return MPQ_ERR_UNSUPPORTED;
+    if (rows < 0 || cols <= 0 || cols % 128 != 0 || ldx < cols)
+        return MPQ_ERR_SHAPE;
+    if (q != nullptr && (ldq < cols || lds < rows))
+        return MPQ_ERR_SHAPE;
+    if (qT != nullptr && (rows % 128 != 0 || ldqT < rows || ldsT < cols))
+        return MPQ_ERR_SHAPE;
+    if (!aligned(x, 16) || ldx % 8 != 0)
+        return MPQ_ERR_ALIGN;
+    if (q != nullptr && (!aligned(q, 16) || ldq % 16 != 0 || !aligned(s, 4)))
+        return MPQ_ERR_ALIGN;
+    if (qT != nullptr && (!aligned(qT, 16) || ldqT % 16 != 0 || !aligned(sT, 4)))
+        return MPQ_ERR_ALIGN;
+    const bool pow2 = (flags & MPQ_POW2) != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
+    if (rows == 0)
+        return MPQ_OK;
+    if (qT == nullptr)
+        return from_cuda(mpq::launch_quant_rows(xb, rows, cols, ldx, q, ldq, s, lds, pow2, h->num_sms, st));
+    return from_cuda(
+        mpq::launch_quant_dual(xb, rows, cols, ldx, q, ldq, s, lds, qT, ldqT, sT, ldsT, pow2, h->num_sms, st));
+}
+
+mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, int64_t cols, int64_t ldw,
+                                   uint8_t *q, int64_t ldq, uint8_t *qT, int64_t ldqT, float *s, int64_t lds,
+                                   uint32_t flags, void *stream)
+{
+    if (h == nullptr || w == nullptr || q == nullptr || s == nullptr)
+        return MPQ_ERR_NULL;
+    if (flags & ~MPQ_POW2)
+        return MPQ_ERR_UNSUPPORTED;
+    if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0 || ldw < cols || ldq < cols ||
+        lds < cols / 128 || (qT != nullptr && ldqT < rows))
+        return MPQ_ERR_SHAPE;
+    if (!aligned(w, 16) || ldw % 8 != 0 || !aligned(q, 16) || ldq % 16 != 0 || !aligned(s, 4) ||
+        (qT != nullptr && (!aligned(qT, 16) || ldqT % 16 != 0)))
+        return MPQ_ERR_ALIGN;
+    if (rows == 0 || cols == 0)
+        return MPQ_OK;
+    return from_cuda(mpq::launch_quant_block(static_cast<const uint16_t *>(w), rows, cols, ldw, q, ldq, qT, ldqT, s,
+                                             lds, (flags & MPQ_POW2) != 0, h->num_sms,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+static mpq_status check_gemm_common(int64_t N, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
+                                    const uint8_t *B, int64_t ldb, const float *sB, void *C, int64_t ldc,
+                                    int out_dtype)
+{
+    if (A == nullptr || sA == nullptr || B == nullptr || sB == nullptr || C == nullptr)
+        return MPQ_ERR_NULL;
+    if (out_dtype != MPQ_OUT_BF16 && out_dtype != MPQ_OUT_FP32)
+        return MPQ_ERR_UNSUPPORTED;
+    if (N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || lda < K || ldb < K || ldc < N)
+        return MPQ_ERR_SHAPE;
+    if (K > (int64_t(1) << 31) || N > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    const int64_t esz = out_dtype == MPQ_OUT_FP32 ? 4 : 2;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || lda % 16 != 0 || ldb % 16 != 0 ||
+        (ldc * esz) % 16 != 0 || !aligned(sA, 4) || !aligned(sB, 4))
+        return MPQ_ERR_ALIGN;
+    return MPQ_OK;
+}
+
+mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int64_t K, const uint8_t *A,
+                                int64_t lda, const float *sA, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                                const float *sB, int64_t ldsb, void *C, int64_t ldc, int out_dtype,
+                                void *stream)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if (op != MPQ_OP_FPROP && op != MPQ_OP_DGRAD && op != MPQ_OP_WGRAD)
+        return MPQ_ERR_UNSUPPORTED;
+    mpq_status st = check_gemm_common(N, K, A, lda, sA, B, ldb, sB, C, ldc, out_dtype);
+    if (st != MPQ_OK)
+        return st;
+    if (M < 0 || M > (int64_t(1) << 31) || ldsa < M)
+        return MPQ_ERR_SHAPE;
+    if ((op == MPQ_OP_FPROP && ldsb < K / 128) || (op == MPQ_OP_DGRAD && ldsb < N / 128) ||
+        (op == MPQ_OP_WGRAD && ldsb < N))
+        return MPQ_ERR_SHAPE;
+    if (M == 0)
+        return MPQ_OK;
+    CUtensorMap tmA, tmB;
+    if ((st = encode_operand(&tmA, A, M, K, lda, 128)) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmB, B, N, K, ldb, 256)) != MPQ_OK)
+        return st;
+    mpq::GemmArgs a{};
+    a.M = M; a.N = N; a.K = K;
+    a.sA = sA; a.ldsa = ldsa;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = 0;
+    a.C = C; a.ldc = ldc;
+    a.offsets = nullptr; a.G = 1;
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
+    return from_cuda(mpq::launch_gemm(tmA, tmB, a, sb, out_dtype == MPQ_OUT_FP32, h->num_sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
+                                        int64_t N, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
+                                        int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB,
+                                        int64_t ldsb, void *C, int64_t ldc, int out_dtype, uint32_t flags,
+                                        void *stream)
+{
+    if (h == nullptr || d_offsets == nullptr)
+        return MPQ_ERR_NULL;
+    if (flags != 0)
+        return MPQ_ERR_UNSUPPORTED;
+    mpq_status st = check_gemm_common(N, K, A, lda, sA, B, ldb, sB, C, ldc, out_dtype);
+    if (st != MPQ_OK)
+        return st;
+    if (G < 1 || G > 1024 || M_total < 0 || M_total > (int64_t(1) << 31) || ldsa < M_total || ldsb < K / 128 ||
+        G * N > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    if (!aligned(d_offsets, 8))
+        return MPQ_ERR_ALIGN;
+    if (M_total == 0)
+        return MPQ_OK;
+    CUtensorMap tmA, tmB;
+    if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmB, B, G * N, K, ldb, 256)) != MPQ_OK)
+        return st;
+    mpq::GemmArgs a{};
+    a.M = M_total; a.N = N; a.K = K;
+    a.sA = sA; a.ldsa = ldsa;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
+    a.C = C; a.ldc = ldc;
+    a.offsets = d_offsets; a.G = static_cast<int>(G);
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    return from_cuda(mpq::launch_gemm(tmA, tmB, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, h->num_sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mpq_status mpq_selftest_wait_timeout(mpq_handle h, uint64_t timeout_ns, void *stream)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    return from_cuda(mpq::launch_wait_selftest(h->d_status, timeout_ns == 0 ? 1000000ull : timeout_ns,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+} // extern "C"

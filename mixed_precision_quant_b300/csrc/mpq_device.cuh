@@ -1,0 +1,359 @@
+// mpq_device.cuh -- sm_103a device helpers: mbarriers with bounded waits, TMA,
+// tcgen05 (TMEM alloc / MMA / commit / load), packed FP32x2 arithmetic, E4M3
+// conversion and the exact group-scale arithmetic shared by the quantizer and the
+// fused decode path.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace mpq {
+
+// Status codes written to the device status word (same values as mpq_status).
+constexpr int kStatusTimeout = 6;
+
+// ---------------------------------------------------------------- addresses
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Shared control block of one CTA: an abort flag every role polls, the caller's
+// device status word and the wait limit.
+struct WaitCtl {
+    volatile int *abort;   // shared memory
+    int *status;           // global: [0] = code, [1] = where (role << 8 | barrier id)
+    uint64_t timeout_ns;
+};
+
+// Bounded wait on a barrier phase.  Returns false when the CTA is aborting, either
+// because another role gave up or because this wait ran past the limit, in which
+// case it records MPQ timeout status and the waiter's tag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &c, int tag)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            if (c.status != nullptr && atomicCAS(c.status, 0, kStatusTimeout) == 0)
+                atomicExch(c.status + 1, tag);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- TMA / cp.async
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled bulk tensor load into shared memory, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int32_t x, int32_t y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 4- or 16-byte asynchronous global->shared copy; bytes past src_bytes are zero-filled.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// The barrier receives one arrival once every cp.async issued so far by this thread lands.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 -> FP32, one CTA.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
+// 8-row core-matrix groups 1024 bytes apart.  The tile base must be 1024-byte aligned; a
+// K offset inside the 128-byte swizzle row is added to the start address.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, bits 0-13
+    d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;                    // swizzle mode: 128-byte
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D = F32, A = B = E4M3, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n)
+{
+    return (1u << 4)                                   // D format: F32
+           | (0u << 7) | (0u << 10)                    // A, B format: E4M3
+           | (static_cast<uint32_t>(n >> 3) << 17)     // N >> 3
+           | (static_cast<uint32_t>(m >> 4) << 24);    // M >> 4
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns; thread i of the warp receives lane
+// (warp's lane quadrant base + i).
+#define MPQ_TMEM_LD32(taddr, r)                                                                   \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                        \
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"                        \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"       \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),        \
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),      \
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),  \
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),  \
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),  \
+                   "=r"(r[30]), "=r"(r[31])                                                       \
+                 : "r"(taddr))
+
+// Wait for this thread's TMEM loads; the registers are tied in so no use moves above it.
+#define MPQ_TMEM_WAIT_LD32(r)                                                                     \
+    asm volatile("tcgen05.wait::ld.sync.aligned;"                                                 \
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),        \
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),      \
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),  \
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
+                   "+r"(r[30]), "+r"(r[31])                                                       \
+                 :                                                                                \
+                 : "memory")
+
+// ---------------------------------------------------------------- packed FP32x2
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
+{
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+__device__ __forceinline__ float lo_of(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_of(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// d = a * b + c on two lanes at once, each rounded once (round to nearest even).
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// ---------------------------------------------------------------- E4M3 conversion
+
+// Two binary32 values -> two E4M3 codes, round to nearest even, saturating to +-448.
+// Byte 0 of the result holds `first`, byte 1 holds `second`.
+__device__ __forceinline__ uint32_t e4m3x2(float first, float second)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_lo(uint32_t w) { return w << 16; }
+__device__ __forceinline__ uint32_t bf16x2_hi(uint32_t w) { return w & 0xFFFF0000u; }
+
+// ---------------------------------------------------------------- group scales
+//
+// A group's scale maps its max-abs value onto the largest E4M3 value 448: s = amax / 448
+// (one IEEE binary32 division), or with power-of-2 scales s = 2^e, e the smallest integer
+// with amax <= 448 * 2^e.  An all-zero group gets s = 1.  Every element becomes the
+// correctly rounded binary32 quotient x / s, then E4M3 round-to-nearest-even.
+
+// 2^e as binary32 for -149 <= e <= 127 (exact, subnormal below -126).
+__device__ __forceinline__ float exp2_int(int e)
+{
+    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                     : __uint_as_float(1u << (e + 149));
+}
+
+// Smallest e with amax <= 448 * 2^e, for finite amax > 0.  With amax = f * 2^E, f in [1, 2):
+// 448 * 2^e = 1.75 * 2^(e + 8), so e = E - 8 when f <= 1.75 and E - 7 otherwise.
+__device__ __forceinline__ int pow2_exponent(float amax)
+{
+    const uint32_t b = __float_as_uint(amax);
+    int E = static_cast<int>((b >> 23) & 0xFF);
+    uint32_t f = b & 0x7FFFFFu;
+    if (E == 0) { // subnormal: normalise the 23-bit fraction
+        const int p = 31 - __clz(f);                 // top set bit, 0..22
+        f = (f << (23 - p)) & 0x7FFFFFu;
+        E = p - 149;
+    } else {
+        E -= 127;
+    }
+    return E - 8 + (f > 0x600000u ? 1 : 0);
+}
+
+struct GroupScale {
+    float s;    // the stored scale
+    float r;    // multiplier used on the fast path
+    int mode;   // 0: r = RN(1/s) with boundary check, 1: r exact (x * r == x / s), 2: divide
+};
+
+__device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
+{
+    GroupScale g;
+    if (amax == 0.0f) {
+        g.s = 1.0f; g.r = 1.0f; g.mode = 1;
+        return g;
+    }
+    if (pow2) {
+        const int e = pow2_exponent(amax);
+        g.s = exp2_int(e);
+        if (e >= -126) { g.r = exp2_int(-e); g.mode = 1; }
+        else { g.r = 0.0f; g.mode = 2; }
+        return g;
+    }
+    g.s = __fdiv_rn(amax, 448.0f);
+    if (g.s < 1.17549435e-38f) { g.r = 0.0f; g.mode = 2; }
+    else { g.r = __frcp_rn(g.s); g.mode = 0; }
+    return g;
+}
+
+// The correctly rounded quotient x / s as far as the E4M3 code is concerned.
+//
+// Method (reciprocal multiply with a boundary test): y = RN(x * RN(1/s)) lies within
+// 2 binary32 ulps of RN(x / s).  The E4M3 code of a binary32 value changes only at the
+// E4M3 rounding boundaries, which in the normal range are the binary32 values whose low
+// 20 fraction bits equal 0x80000.  When y is more than 3 ulps from such a value, y and
+// RN(x / s) give the same code; otherwise, and in the E4M3 subnormal range
+// [2^-11, 2^-6), the quotient is recomputed with the IEEE division.  Below 2^-11 both
+// round to a signed zero.
+__device__ __forceinline__ float scaled_value(float x, const GroupScale &g)
+{
+    if (g.mode == 1)
+        return x * g.r;
+    if (g.mode == 2)
+        return __fdiv_rn(x, g.s);
+    const float y = x * g.r;
+    const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
+    const bool sub = (b >= 0x3A000000u) && (b < 0x3C800000u);
+    const bool near = ((b & 0xFFFFFu) - 0x7FFFDu) < 7u;
+    if (sub || near)
+        return __fdiv_rn(x, g.s);
+    return y;
+}
+
+} // namespace mpq

@@ -1,0 +1,48 @@
+// mpq_internal.h -- launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mpq {
+
+cudaError_t launch_quant_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+                              int64_t ldq, float *s, int64_t lds, bool pow2, int num_sms, cudaStream_t st);
+
+cudaError_t launch_quant_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+                              int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sT,
+                              int64_t ldsT, bool pow2, int num_sms, cudaStream_t st);
+
+cudaError_t launch_quant_block(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw, uint8_t *q,
+                               int64_t ldq, uint8_t *qT, int64_t ldqT, float *s, int64_t lds, bool pow2,
+                               int num_sms, cudaStream_t st);
+
+// Which B-side scale layout the GEMM reads (see fp8_gemm_blockscaled in mpq.h).
+enum ScaleB : int { kScaleBlockNK = 0, kScaleBlockKN = 1, kScaleRowKN = 2 };
+
+struct GemmArgs {
+    int64_t M, N, K;            // rows of C, columns of C, reduction length
+    const float *sA;            // [K/128][ldsa]
+    int64_t ldsa;
+    const float *sB;
+    int64_t ldsb;
+    int64_t sb_group_stride;    // elements between experts' B scales (grouped)
+    void *C;
+    int64_t ldc;
+    const int64_t *offsets;     // grouped: device [G+1] row offsets, else null
+    int G;                      // grouped: number of experts, else 1
+    int *status;                // device status word (2 ints)
+    uint64_t timeout_ns;
+};
+
+// Block-scaled FP8 GEMM on tcgen05: C[M,N] = sum over 128-wide K slices of
+// (A_slice B_slice^T) * sA * sB, promoted into FP32 after every slice.
+// tmA covers A [rows, K] E4M3, tmB covers B [rows, K] E4M3 (both K-major, 128B swizzle).
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, int scale_b,
+                        bool out_fp32, int num_sms, cudaStream_t st);
+
+// Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
+cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);
+
+} // namespace mpq

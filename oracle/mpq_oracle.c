@@ -9,8 +9,8 @@
  *
  * What it follows (the source pages are scraped copies of the FP8 mixed-precision
  * training description of an MoE LLM technical report):
- *   - "DeepSeek ... FP8 mixed precision" page 1 (xn--9g3bo1gtkw0l8ubf92bgle.kr qna
- *     131281), second paragraph: the scaling factor is derived from the online
+ *   - page 1 (xn--9g3bo1gtkw0l8ubf92bgle.kr, qna board post 131281), second
+ *     paragraph: the scaling factor is derived from the online
  *     maximum absolute value and the activation or weight is quantized online into
  *     FP8; FP8 GEMMs take FP8 inputs and produce BF16 or FP32 outputs.
  *   - page 3 (blog.cameseeing.com freeboard 1171527), first paragraph: the input
@@ -23,8 +23,9 @@
  *     second paragraph: integral power-of-2 scaling factors.
  *   - The E4M3 format itself (bias 7, no infinities, S.1111.111 = NaN, largest
  *     finite 448) is the OCP 8-bit floating point specification; the group shapes
- *     1x128 (activations) and 128x128 (weights) and "scale = amax / 448" are the
- *     task statement's reading of the pages' lost subscripts.
+ *     1x128 (activations) and 128x128 (weights) and "scale = amax / 448" read the
+ *     subscripts the scraped pages lost (their text keeps only "128 elements" and
+ *     "128x1 tiles").
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - rounding of the cast is round-to-nearest-even, overflow saturates to +-448;
@@ -229,6 +230,19 @@ static double scale_b(int op, const float *sB, int64_t ldsb, int64_t n, int64_t 
     return (double)sB[(k / 128) * ldsb + n];
 }
 
+/* All 256 decoded codes, filled once from mpqo_e4m3_decode (lookup for speed only). */
+static double g_dec[256];
+static int g_dec_ready = 0;
+
+static void init_dec(void)
+{
+    if (g_dec_ready)
+        return;
+    for (int c = 0; c < 256; ++c)
+        g_dec[c] = mpqo_e4m3_decode((uint8_t)c);
+    g_dec_ready = 1;
+}
+
 /* One output element: sum over k of (dec(A[m,k]) sA) (dec(B[n,k]) sB), in FP64,
  * in k order, plus the sum of magnitudes of the terms (for the tolerance). */
 static void dot_one(int op, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
@@ -236,9 +250,10 @@ static void dot_one(int op, int64_t K, const uint8_t *A, int64_t lda, const floa
                     int64_t ldsb, int64_t m, int64_t n, double *ref, double *absref)
 {
     double acc = 0.0, aacc = 0.0;
+    init_dec();
     for (int64_t k = 0; k < K; ++k) {
-        double a = mpqo_e4m3_decode(A[m * lda + k]) * (double)sA[(k / 128) * ldsa + m];
-        double b = mpqo_e4m3_decode(B[n * ldb + k]) * scale_b(op, sB, ldsb, n, k);
+        double a = g_dec[A[m * lda + k]] * (double)sA[(k / 128) * ldsa + m];
+        double b = g_dec[B[n * ldb + k]] * scale_b(op, sB, ldsb, n, k);
         acc += a * b;
         aacc += fabs(a * b);
     }

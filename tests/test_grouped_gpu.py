@@ -1,0 +1,119 @@
+"""GPU parity of the grouped (MoE expert) block-scaled FP8 GEMM against the FP64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._util import assert_gemm_close, bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mpq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixed_precision_quant_b300 as m
+    return m
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _experts(G, N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    qs, ss = [], []
+    for _ in range(G):
+        w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16)
+        q, _, s = oracle.quant_block_128x128(bf16_bits(w))
+        qs.append(q); ss.append(s)
+    return np.stack(qs), np.stack(ss)
+
+
+@pytest.mark.parametrize("counts,lead,trail", [
+    ([3, 0, 130, 1, 200], 0, 0),
+    ([0, 0, 0, 257], 5, 7),
+    ([128, 128], 0, 0),
+    ([1] * 40, 3, 0),
+])
+def test_grouped_small(mpq, counts, lead, trail):
+    G, N, K = len(counts), 256, 384
+    off = np.concatenate([[0], np.cumsum(counts)]) + lead
+    M = int(off[-1]) + trail
+    g = torch.Generator().manual_seed(sum(counts))
+    a = (torch.randn((M, K), generator=g)).to(torch.bfloat16)
+    qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
+    qb, sb = _experts(G, N, K, 7 + G)
+    C = torch.full((M, N), 12345.0, dtype=torch.float32, device="cuda")
+    mpq.fp8_grouped_gemm_blockscaled(_dev(off.astype(np.int64)), _dev(qa), _dev(sa), _dev(qb), _dev(sb),
+                                     out_dtype=mpq.OUT_FP32, C=C)
+    ref, absref = oracle.grouped_gemm_ref(off, qa, sa, qb, sb)
+    got = C.cpu().numpy().astype(np.float64)
+    rows = np.zeros(M, bool)
+    rows[off[0]:off[-1]] = True
+    assert_gemm_close(got[rows], ref[rows], absref[rows], "grouped")
+    assert np.all(got[~rows] == 12345.0), "rows outside every expert were written"
+
+
+def test_grouped_equals_single_gemms(mpq):
+    """Cross-path invariant: each expert's rows equal a single-GEMM call, bit for bit."""
+    counts = [70, 300, 0, 129]
+    G, N, K = len(counts), 384, 256
+    off = np.concatenate([[0], np.cumsum(counts)])
+    M = int(off[-1])
+    g = torch.Generator().manual_seed(99)
+    a = (torch.randn((M, K), generator=g) * 3).to(torch.bfloat16)
+    qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
+    qb, sb = _experts(G, N, K, 5)
+    C = mpq.fp8_grouped_gemm_blockscaled(_dev(off.astype(np.int64)), _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    for e in range(G):
+        if counts[e] == 0:
+            continue
+        r = slice(int(off[e]), int(off[e + 1]))
+        Ce = mpq.fp8_gemm_blockscaled(mpq.FPROP, _dev(qa[r]), _dev(np.ascontiguousarray(sa[:, r])), _dev(qb[e]),
+                                      _dev(sb[e]))
+        assert torch.equal(C[r], Ce), f"expert {e}"
+
+
+def _sampled_moe_check(mpq, d, proj, pow2_input):
+    """Run one projection on the GPU end to end (quantize rows 1x128 + grouped GEMM) and
+    check sampled rows of three experts (largest, median, smallest non-empty) against the
+    oracle run from the same BF16 inputs."""
+    off = d["offsets"]
+    X = d["X_up"] if proj == "up" else d["X_dn"]
+    Wt = d["W_up"] if proj == "up" else d["W_dn"]
+    G, N, K = Wt.shape
+    qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X, pow2=pow2_input)
+    qw = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    for e in range(G):
+        mpq.fp8_quant_block_128x128(Wt[e], q=qw[e], s=sw[e])
+    C = mpq.fp8_grouped_gemm_blockscaled(off.cuda(), qx, sx, qw, sw)
+    torch.cuda.synchronize()
+    counts = d["counts"].numpy()
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz])]
+    rng = np.random.default_rng(5)
+    for e in (order[-1], order[len(order) // 2], order[0]):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        rows = np.unique(np.concatenate([rng.integers(r0, r1, 12), [r0, r1 - 1]]))
+        oq, os_ = oracle.quant_tile_1x128(bf16_bits(X[torch.from_numpy(rows).cuda()]), pow2=pow2_input)
+        nb = int(rng.integers(0, N // 128))
+        oqw, _, osw = oracle.quant_block_128x128(bf16_bits(Wt[e, nb * 128:(nb + 1) * 128]))
+        ref, absref = oracle.gemm_ref(oracle.FPROP, oq, os_, oqw, osw)
+        got = C[torch.from_numpy(rows).cuda(), nb * 128:(nb + 1) * 128].float().cpu().numpy().astype(np.float64)
+        assert_gemm_close(got, ref, absref, f"{proj} expert {e}")
+
+
+def test_moe_prefill_full_size_sampled(mpq):
+    d = workloads.moe_prefill(device="cuda")
+    _sampled_moe_check(mpq, d, "up", False)
+    _sampled_moe_check(mpq, d, "down", True)
+
+
+def test_moe_decode_full_size_sampled(mpq):
+    d = workloads.moe_decode(device="cuda")
+    _sampled_moe_check(mpq, d, "up", False)
+    _sampled_moe_check(mpq, d, "down", True)
