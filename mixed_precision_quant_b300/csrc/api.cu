@@ -59,6 +59,23 @@ mpq_status encode_operand(CUtensorMap *m, const uint8_t *ptr, int64_t rows, int6
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
+// 2-D BF16 source view [rows, cols] (cols contiguous), box 128 columns x box_rows, no
+// swizzle, out-of-bounds rows read as zero.
+mpq_status encode_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return MPQ_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
+}
+
 mpq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPQ_OK : MPQ_ERR_CUDA; }
 
 } // namespace
@@ -160,15 +177,24 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
         return MPQ_ERR_ALIGN;
     if (qT != nullptr && (!aligned(qT, 16) || ldqT % 16 != 0 || !aligned(sT, 4)))
         return MPQ_ERR_ALIGN;
-    const bool pow2 = (flags & MPQ_POW2) != 0;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint16_t *xb = static_cast<const uint16_t *>(x);
     if (rows == 0)
         return MPQ_OK;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    const bool pow2 = (flags & MPQ_POW2) != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mpq::QuantArgs a{};
+    a.rows = rows; a.cols = cols;
+    a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
+    a.qT = qT; a.ldqT = ldqT; a.sT = sT; a.ldsT = ldsT;
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tm;
+    mpq_status e = encode_bf16(&tm, x, rows, cols, ldx, qT == nullptr ? 64 : 128);
+    if (e != MPQ_OK)
+        return e;
     if (qT == nullptr)
-        return from_cuda(mpq::launch_quant_rows(xb, rows, cols, ldx, q, ldq, s, lds, pow2, h->num_sms, st));
-    return from_cuda(
-        mpq::launch_quant_dual(xb, rows, cols, ldx, q, ldq, s, lds, qT, ldqT, sT, ldsT, pow2, h->num_sms, st));
+        return from_cuda(mpq::launch_quant_rows(tm, a, pow2, h->num_sms, st));
+    return from_cuda(mpq::launch_quant_dual(tm, a, pow2, h->num_sms, st));
 }
 
 mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, int64_t cols, int64_t ldw,
@@ -187,8 +213,18 @@ mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, in
         return MPQ_ERR_ALIGN;
     if (rows == 0 || cols == 0)
         return MPQ_OK;
-    return from_cuda(mpq::launch_quant_block(static_cast<const uint16_t *>(w), rows, cols, ldw, q, ldq, qT, ldqT, s,
-                                             lds, (flags & MPQ_POW2) != 0, h->num_sms,
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    mpq::QuantArgs a{};
+    a.rows = rows; a.cols = cols;
+    a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
+    a.qT = qT; a.ldqT = ldqT;
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tm;
+    mpq_status e = encode_bf16(&tm, w, rows, cols, ldw, 128);
+    if (e != MPQ_OK)
+        return e;
+    return from_cuda(mpq::launch_quant_block(tm, a, (flags & MPQ_POW2) != 0, h->num_sms,
                                              static_cast<cudaStream_t>(stream)));
 }
 

@@ -307,53 +307,75 @@ __device__ __forceinline__ int pow2_exponent(float amax)
 }
 
 struct GroupScale {
-    float s;    // the stored scale
-    float r;    // multiplier used on the fast path
-    int mode;   // 0: r = RN(1/s) with boundary check, 1: r exact (x * r == x / s), 2: divide
+    float s;     // the stored scale
+    float rlo;   // multipliers bracketing the quotient (see e4m3_pair), or the exact
+    float rhi;   //   multiplier 2^-e when the scale is a power of two
+    int mode;    // 0: bracket, 1: exact multiplier, 2: divide
 };
 
+// Scale of a group from its max-abs value.
 __device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
 {
     GroupScale g;
     if (amax == 0.0f) {
-        g.s = 1.0f; g.r = 1.0f; g.mode = 1;
+        g.s = 1.0f; g.rlo = 1.0f; g.rhi = 1.0f; g.mode = 1;
         return g;
     }
     if (pow2) {
         const int e = pow2_exponent(amax);
         g.s = exp2_int(e);
-        if (e >= -126) { g.r = exp2_int(-e); g.mode = 1; }
-        else { g.r = 0.0f; g.mode = 2; }
+        if (e >= -126) { g.rlo = g.rhi = exp2_int(-e); g.mode = 1; }
+        else { g.rlo = g.rhi = 0.0f; g.mode = 2; }
         return g;
     }
     g.s = __fdiv_rn(amax, 448.0f);
-    if (g.s < 1.17549435e-38f) { g.r = 0.0f; g.mode = 2; }
-    else { g.r = __frcp_rn(g.s); g.mode = 0; }
+    if (g.s < 1.17549435e-38f) {
+        g.rlo = g.rhi = 0.0f; g.mode = 2;
+        return g;
+    }
+    const float r = __frcp_rn(g.s);
+    g.rlo = __fmul_rn(r, 1.0f - 0x1p-21f);
+    g.rhi = __fmul_rn(r, 1.0f + 0x1p-21f);
+    g.mode = 0;
     return g;
 }
 
-// The correctly rounded quotient x / s as far as the E4M3 code is concerned.
+// IEEE binary32 division, kept out of line: it only runs for the rare values the bracket
+// cannot decide and for subnormal scales.
+static __device__ __noinline__ float exact_quotient(float x, float s) { return __fdiv_rn(x, s); }
+
+// E4M3 codes of the binary32 quotients x0 / s and x1 / s (each correctly rounded to
+// binary32, then rounded to nearest even E4M3 with saturation); byte 0 = x0.
 //
-// Method (reciprocal multiply with a boundary test): y = RN(x * RN(1/s)) lies within
-// 2 binary32 ulps of RN(x / s).  The E4M3 code of a binary32 value changes only at the
-// E4M3 rounding boundaries, which in the normal range are the binary32 values whose low
-// 20 fraction bits equal 0x80000.  When y is more than 3 ulps from such a value, y and
-// RN(x / s) give the same code; otherwise, and in the E4M3 subnormal range
-// [2^-11, 2^-6), the quotient is recomputed with the IEEE division.  Below 2^-11 both
-// round to a signed zero.
-__device__ __forceinline__ float scaled_value(float x, const GroupScale &g)
+// Method (bracketing by monotonicity): with r = RN(1/s), the products
+// lo = RN(x * RN(r (1 - 2^-21))) and hi = RN(x * RN(r (1 + 2^-21))) satisfy
+// |lo| <= |RN(x / s)| <= |hi|, because the exact products differ from x / s by a relative
+// factor in (1 - 2^-21 - 2^-22, 1 - 2^-22) and (1 + 2^-22, 1 + 2^-21 + 2^-22) and
+// rounding to nearest is monotone.  Rounding binary32 to E4M3 is monotone too, so when
+// lo and hi give the same code, every value between them -- RN(x / s) included -- gives
+// that code.  Otherwise (a quotient within about 3 binary32 ulps of an E4M3 rounding
+// boundary) the quotient is recomputed with the IEEE division.  For power-of-2 scales
+// x * 2^-e is the quotient itself (mode 1).
+__device__ __forceinline__ uint32_t e4m3_pair(float x0, float x1, const GroupScale &g)
 {
-    if (g.mode == 1)
-        return x * g.r;
     if (g.mode == 2)
-        return __fdiv_rn(x, g.s);
-    const float y = x * g.r;
-    const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
-    const bool sub = (b >= 0x3A000000u) && (b < 0x3C800000u);
-    const bool near = ((b & 0xFFFFFu) - 0x7FFFDu) < 7u;
-    if (sub || near)
-        return __fdiv_rn(x, g.s);
-    return y;
+        return e4m3x2(exact_quotient(x0, g.s), exact_quotient(x1, g.s));
+    const unsigned long long x = pack2(x0, x1);
+    const unsigned long long lo = fmul2(x, pack2(g.rlo, g.rlo));
+    if (g.mode == 1)
+        return e4m3x2(lo_of(lo), hi_of(lo));
+    const unsigned long long hi = fmul2(x, pack2(g.rhi, g.rhi));
+    const uint32_t clo = e4m3x2(lo_of(lo), hi_of(lo));
+    const uint32_t chi = e4m3x2(lo_of(hi), hi_of(hi));
+    if (__builtin_expect(clo == chi, 1))
+        return clo;
+    return e4m3x2(exact_quotient(x0, g.s), exact_quotient(x1, g.s));
+}
+
+// Single-value form (code in the low byte).
+__device__ __forceinline__ uint32_t e4m3_one(float x, const GroupScale &g)
+{
+    return e4m3_pair(x, 0.0f, g) & 0xFFu;
 }
 
 } // namespace mpq

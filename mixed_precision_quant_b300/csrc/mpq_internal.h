@@ -7,16 +7,26 @@
 
 namespace mpq {
 
-cudaError_t launch_quant_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
-                              int64_t ldq, float *s, int64_t lds, bool pow2, int num_sms, cudaStream_t st);
+// Quantizer arguments.  The BF16 source is read through a 2-D TMA view (tensor map)
+// encoded by the caller: [rows, cols] with box 128 columns x (64 rows for the row
+// quantizer, 128 rows for the dual and block quantizers).
+struct QuantArgs {
+    int64_t rows, cols;
+    uint8_t *q;         // row-wise (or block) codes [rows, cols], ldq
+    int64_t ldq;
+    float *s;           // row-wise scales [cols/128][lds] or block scales [rows/128][lds]
+    int64_t lds;
+    uint8_t *qT;        // transposed codes [cols, rows], ldqT (optional)
+    int64_t ldqT;
+    float *sT;          // column-group scales [rows/128][ldsT]
+    int64_t ldsT;
+    int *status;        // device status word
+    uint64_t timeout_ns;
+};
 
-cudaError_t launch_quant_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
-                              int64_t ldq, float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sT,
-                              int64_t ldsT, bool pow2, int num_sms, cudaStream_t st);
-
-cudaError_t launch_quant_block(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw, uint8_t *q,
-                               int64_t ldq, uint8_t *qT, int64_t ldqT, float *s, int64_t lds, bool pow2,
-                               int num_sms, cudaStream_t st);
+cudaError_t launch_quant_rows(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_dual(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_block(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
 
 // Which B-side scale layout the GEMM reads (see fp8_gemm_blockscaled in mpq.h).
 enum ScaleB : int { kScaleBlockNK = 0, kScaleBlockKN = 1, kScaleRowKN = 2 };
