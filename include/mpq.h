@@ -87,6 +87,12 @@ mpq_status mpq_destroy(mpq_handle h);
  * (default 1e9).  0 restores the default. */
 mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
 
+/* Data sharing of the GEMM entry points issued through this handle.  1 (default): CTAs
+ * run as 2-CTA clusters on neighbouring SMs whose 128 x 256 output tiles share the same
+ * B (weight) rows; each CTA loads half of the B slice and multicasts it to both.  0: every
+ * CTA loads its own operands.  The results are bit-identical. */
+mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
+
 /* Synchronize `stream`, read and clear the device status word.  Returns MPQ_OK or the
  * recorded error (MPQ_ERR_TIMEOUT); *where_out (may be NULL) receives the tag of the
  * wait that gave up (role << 8 | barrier index), 0 if none. */

@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "mpq_create": (INT, [ctypes.POINTER(P)]),
         "mpq_destroy": (INT, [P]),
         "mpq_set_wait_timeout": (INT, [P, U64]),
+        "mpq_set_gemm_cta_pair": (INT, [P, INT]),
         "mpq_check_device_status": (INT, [P, P, ctypes.POINTER(INT)]),
         "fp8_quant_tile_1x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, P, I, U32, P]),
         "fp8_quant_block_128x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
@@ -232,6 +233,12 @@ def mpq_check_device_status(device=None, stream=None):
 def mpq_set_wait_timeout(timeout_ns: int, device=None):
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     _check("mpq_set_wait_timeout", _lib.mpq_set_wait_timeout(_handle(dev), int(timeout_ns)))
+
+
+def mpq_set_gemm_cta_pair(enable: bool, device=None):
+    """Run GEMM tiles on SM pairs (True, default) or single SMs (False)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    _check("mpq_set_gemm_cta_pair", _lib.mpq_set_gemm_cta_pair(_handle(dev), int(bool(enable))))
 
 
 def mpq_selftest_wait_timeout(timeout_ns: int = 1_000_000, device=None, stream=None):

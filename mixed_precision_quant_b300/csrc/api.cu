@@ -14,6 +14,7 @@ struct mpq_handle_s {
     int num_sms;
     int *d_status;          // [0] code, [1] tag of the wait that gave up
     uint64_t timeout_ns;
+    bool gemm_pair;         // GEMMs on CTA pairs (cta_group::2, 256 x 256 tiles)
 };
 
 namespace {
@@ -76,6 +77,25 @@ mpq_status encode_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t co
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
+// GEMM output view [rows, cols] (cols contiguous, BF16 or FP32), box 64 bytes x 32 rows,
+// 64-byte swizzle (the layout of the kernel's staging buffers); stores are clipped at the
+// tensor bounds.
+mpq_status encode_output(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return MPQ_ERR_CUDA;
+    const int64_t esz = fp32 ? 4 : 2;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esz)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
+}
+
 mpq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPQ_OK : MPQ_ERR_CUDA; }
 
 } // namespace
@@ -118,6 +138,7 @@ mpq_status mpq_create(mpq_handle *out)
         return MPQ_ERR_CUDA;
     }
     h->timeout_ns = kDefaultTimeoutNs;
+    h->gemm_pair = true;
     *out = h;
     return MPQ_OK;
 }
@@ -137,6 +158,14 @@ mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns)
     if (h == nullptr)
         return MPQ_ERR_NULL;
     h->timeout_ns = timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns;
+    return MPQ_OK;
+}
+
+mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    h->gemm_pair = enable != 0;
     return MPQ_OK;
 }
 
@@ -269,7 +298,10 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     CUtensorMap tmA, tmB;
     if ((st = encode_operand(&tmA, A, M, K, lda, 128)) != MPQ_OK)
         return st;
-    if ((st = encode_operand(&tmB, B, N, K, ldb, 256)) != MPQ_OK)
+    if ((st = encode_operand(&tmB, B, N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
+        return st;
+    CUtensorMap tmC;
+    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
         return st;
     mpq::GemmArgs a{};
     a.M = M; a.N = N; a.K = K;
@@ -279,7 +311,7 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     a.offsets = nullptr; a.G = 1;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
-    return from_cuda(mpq::launch_gemm(tmA, tmB, a, sb, out_dtype == MPQ_OUT_FP32, h->num_sms,
+    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, h->gemm_pair, h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -306,7 +338,10 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     CUtensorMap tmA, tmB;
     if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
         return st;
-    if ((st = encode_operand(&tmB, B, G * N, K, ldb, 256)) != MPQ_OK)
+    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
+        return st;
+    CUtensorMap tmC;
+    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
         return st;
     mpq::GemmArgs a{};
     a.M = M_total; a.N = N; a.K = K;
@@ -315,7 +350,8 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     a.C = C; a.ldc = ldc;
     a.offsets = d_offsets; a.G = static_cast<int>(G);
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    return from_cuda(mpq::launch_gemm(tmA, tmB, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, h->num_sms,
+    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, h->gemm_pair,
+                                      h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -12,54 +12,71 @@
 //   block [N/128][K/128] (Fprop), block [K/128][N/128] (Dgrad through the
 //   transposed weight), per-row [K/128][N] (Wgrad, 128x1 token tiles).
 //
-// Design (B300, one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: A 128x128 and B 256x128 E4M3 slices into a 4-stage ring
-//               (128-byte swizzle), one mbarrier per stage;
-//   warp 1      MMA issuer: four tcgen05.mma (M=128, N=256, K=32) per 128-K slice into
-//               one of two TMEM partial buffers (2 x 256 columns), committed per slice;
+// Design (B300, persistent, one CTA per SM, 128 x 256 output tile per CTA).  Two modes:
+//   pair   (default) a cluster of two CTAs on two SMs works on vertically adjacent tiles
+//          that share the same 256 rows of B: each CTA loads its own 128 rows of A and
+//          one half (128 rows) of B per 128-K slice and multicasts that half into both
+//          CTAs' shared memory, so each SM pulls 32 KB per slice from L2 instead of 48 KB.
+//          A stage is refilled only when both CTAs' MMAs released it (commit multicast to
+//          both); everything else (MMA, TMEM hand-off, promotion) stays on each SM.
+//   single one CTA loads all of its A and B slices itself.
+// Roles in each CTA:
+//   warp 0      TMA producer: E4M3 slices into a shared-memory ring (128-byte swizzle);
+//   warp 1      MMA issuer: four MMAs (K = 32 each) per 128-K slice into one of two TMEM
+//               partial buffers (2 x 256 columns), committed per slice;
 //   warp 2      scale loader: cp.async of the slice's A and B scales into an 8-slot ring;
-//   warps 4-11  promotion: tcgen05.ld the slice partial, multiply by its two scales and
-//               accumulate into FP32 registers with packed FP32x2 FMAs, then write the
-//               tile as BF16 or FP32.  Promotion of slice k overlaps the MMAs of k+1.
-// Every wait is bounded; on expiry the CTA records a timeout in the status word,
-// drains its copies and MMAs, frees TMEM and exits.
+//   warps 4-11  promotion: tcgen05.ld the slice partial (two loads in flight), multiply
+//               by its two scales and accumulate into FP32 registers with packed FP32x2
+//               FMAs; promotion of slice k overlaps the MMAs of slice k+1.  The finished
+//               tile is written as BF16 or FP32 through a 2 KB swizzled staging buffer per
+//               warp and TMA bulk-tensor stores (32 rows x 64 bytes per store).
+// Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
+// its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
 
 namespace mpq {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
-constexpr int SSLOTS = 8;
+constexpr int BK = 128;              // K per promotion slice
+constexpr int BN = 256;              // output columns per tile
+constexpr int SSLOTS = 4;            // scale ring depth (slices)
+constexpr uint32_t STAGE_OUT = 2048; // output staging bytes per promotion warp (32 rows x 64 B)
 constexpr int kThreads = 384;
-constexpr uint32_t A_BYTES = BM * BK;
-constexpr uint32_t B_BYTES = BN * BK;
-constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_BYTES = 128 * BK;     // 128 rows of A per CTA per slice
+constexpr uint32_t TMEM_COLS = 512;        // two 256-column partial buffers
 constexpr int kMaxGroups = 1024;
 
-// Barrier indices inside the barrier array.
-constexpr int BAR_FULL = 0;
-constexpr int BAR_EMPTY = BAR_FULL + STAGES;
-constexpr int BAR_TFULL = BAR_EMPTY + STAGES;
-constexpr int BAR_TEMPTY = BAR_TFULL + 2;
-constexpr int BAR_SFULL = BAR_TEMPTY + 2;
-constexpr int BAR_SEMPTY = BAR_SFULL + SSLOTS;
-constexpr int BAR_DRAIN = BAR_SEMPTY + SSLOTS;
-constexpr int NBARS = BAR_DRAIN + 1;
+template <bool PAIR>
+struct Cfg {
+    static constexpr int STAGES = 4;
+    static constexpr int B_ROWS = PAIR ? 128 : 256;          // B rows loaded by one CTA per slice
+    static constexpr uint32_t B_BYTES = BN * BK;             // the full B slice in each CTA
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TILE_M = PAIR ? 256 : 128;          // rows per tile (both CTAs of a pair)
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = BAR_FULL + STAGES;
+    static constexpr int BAR_TFULL = BAR_EMPTY + STAGES;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + 2;
+    static constexpr int BAR_SFULL = BAR_TEMPTY + 2;
+    static constexpr int BAR_SEMPTY = BAR_SFULL + SSLOTS;
+    static constexpr int BAR_DRAIN = BAR_SEMPTY + SSLOTS;
+    static constexpr int NBARS = BAR_DRAIN + 1;
+    static constexpr size_t SMEM_MAIN = STAGES * STAGE_BYTES + 8 * STAGE_OUT + SSLOTS * (128 + BN) * sizeof(float) +
+                                        NBARS * sizeof(uint64_t) + 16;
+};
 
-constexpr size_t kSmemMain = STAGES * (A_BYTES + B_BYTES) + SSLOTS * (BM + BN) * sizeof(float) +
-                             NBARS * sizeof(uint64_t) + 16;
-constexpr size_t kSmemGroups = (kMaxGroups + 1) * (sizeof(int64_t) + sizeof(int)) + 16;
+constexpr size_t kSmemGroups = (kMaxGroups + 1) * 2 * sizeof(int) + 16;
 
-size_t smem_bytes(bool grouped) { return 1024 + kSmemMain + (grouped ? kSmemGroups : 0); }
+template <bool PAIR>
+size_t smem_bytes(bool grouped) { return 1024 + Cfg<PAIR>::SMEM_MAIN + (grouped ? kSmemGroups : 0); }
 
 // Sizes are validated on the host to stay below 2^31 rows / columns.
 struct Tile {
-    int row0;         // first row of A / C
-    int row_end;      // one past the last valid row of this tile
-    int brow0;        // first row of B in the TMA view ([G*N, K] when grouped)
-    int n0;           // first output column
+    int row0;         // first row of A / C handled by this CTA
+    int row_end;      // one past the last valid row for this CTA
+    int brow0;        // first row of B loaded by this CTA (TMA view [G*N, K] when grouped)
+    int n0;           // first output column of the tile
     int64_t sb_base;  // offset of this expert's B scales
 };
 
@@ -73,26 +90,50 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     return true;
 }
 
-template <int SCALE_B, bool OUT_F32, bool GROUPED>
+// acc[16 * c + q] += partial columns (32 c + 2q, 32 c + 2q + 1) scaled, for one 32-column chunk.
+template <int SCALE_B>
+__device__ __forceinline__ void promote_chunk(unsigned long long (&acc)[64], const uint32_t (&v)[32], int c,
+                                              unsigned long long sc2, unsigned long long sa2, const float *sbcol)
+{
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const unsigned long long pv = (static_cast<unsigned long long>(v[2 * q + 1]) << 32) | v[2 * q];
+        if (SCALE_B == kScaleRowKN) {
+            const unsigned long long sb2 = *reinterpret_cast<const unsigned long long *>(sbcol + c * 32 + 2 * q);
+            acc[c * 16 + q] = ffma2(fmul2(pv, sb2), sa2, acc[c * 16 + q]);
+        } else {
+            acc[c * 16 + q] = ffma2(pv, sc2, acc[c * 16 + q]);
+        }
+    }
+}
+
+template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs p)
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs p)
 {
+    using C = Cfg<PAIR>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *smA = base;
     uint8_t *smB = smA + STAGES * A_BYTES;
-    float *ssa = reinterpret_cast<float *>(smB + STAGES * B_BYTES);
-    float *ssb = ssa + SSLOTS * BM;
+    uint8_t *smO = smB + STAGES * C::B_BYTES;                    // output staging, 8 x 2 KB
+    float *ssa = reinterpret_cast<float *>(smO + 8 * STAGE_OUT);
+    float *ssb = ssa + SSLOTS * 128;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ssb + SSLOTS * BN);
-    uint32_t *misc = reinterpret_cast<uint32_t *>(bars + NBARS);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
-    int64_t *goff = reinterpret_cast<int64_t *>(misc + 4);   // grouped: clamped offsets [G+1]
-    int *gtile = reinterpret_cast<int *>(goff + kMaxGroups + 1);  // grouped: first tile of expert
+    int *goff = reinterpret_cast<int *>(misc + 4);                // grouped: clamped offsets [G+1]
+    int *gtile = goff + kMaxGroups + 1;                           // grouped: first tile of expert
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;   // position in the CTA pair
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     const int64_t M = p.M, N = p.N;
     const int KB = static_cast<int>(p.K / BK);
@@ -100,24 +141,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(BAR_FULL + s), 1);
-            mbar_init(bar(BAR_EMPTY + s), 1);
+            mbar_init(bar(C::BAR_FULL + s), 1);
+            mbar_init(bar(C::BAR_EMPTY + s), PAIR ? 2 : 1);   // both CTAs' MMAs release a stage
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(BAR_TFULL + b), 1);
-            mbar_init(bar(BAR_TEMPTY + b), 8);
+            mbar_init(bar(C::BAR_TFULL + b), 1);
+            mbar_init(bar(C::BAR_TEMPTY + b), 8);
         }
         for (int j = 0; j < SSLOTS; ++j) {
-            mbar_init(bar(BAR_SFULL + j), 32);
-            mbar_init(bar(BAR_SEMPTY + j), 8);
+            mbar_init(bar(C::BAR_SFULL + j), 32);
+            mbar_init(bar(C::BAR_SEMPTY + j), 8);
         }
-        mbar_init(bar(BAR_DRAIN), 1);
+        mbar_init(bar(C::BAR_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -125,25 +167,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (GROUPED && warp == 2) {
         // Expert schedule: offsets clamped into [0, M] and made monotone (running max),
-        // then the exclusive prefix sum of m-tiles per expert, times the n-tile count.
+        // then the exclusive prefix sum of (pair) m-tiles per expert, times the n-tiles.
         const int G = p.G;
         for (int g = lane; g <= G; g += 32) {
             const int64_t o = p.offsets[g];
-            goff[g] = o < 0 ? 0 : (o > M ? M : o);
+            goff[g] = static_cast<int>(o < 0 ? 0 : (o > M ? M : o));
         }
         __syncwarp();
         const int per = (G + 1 + 31) / 32;
         const int c0 = lane * per, c1 = c0 + per < G + 1 ? c0 + per : G + 1;
-        int64_t mx = 0;
+        int mx = 0;
         for (int g = c0; g < c1; ++g)
             mx = goff[g] > mx ? goff[g] : mx;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t v = __shfl_up_sync(0xffffffffu, mx, o);
+            const int v = __shfl_up_sync(0xffffffffu, mx, o);
             if (lane >= o && v > mx)
                 mx = v;
         }
-        int64_t run = __shfl_up_sync(0xffffffffu, mx, 1);
+        int run = __shfl_up_sync(0xffffffffu, mx, 1);
         if (lane == 0)
             run = 0;
         for (int g = c0; g < c1; ++g) {
@@ -155,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e0 = lane * perg, e1 = e0 + perg < G ? e0 + perg : G;
         int cnt = 0;
         for (int g = e0; g < e1; ++g)
-            cnt += static_cast<int>((goff[g + 1] - goff[g] + BM - 1) / BM);
+            cnt += static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -166,25 +208,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ex = incl - cnt;
         for (int g = e0; g < e1; ++g) {
             gtile[g] = ex * NT;
-            ex += static_cast<int>((goff[g + 1] - goff[g] + BM - 1) / BM);
+            ex += static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
         }
         if (lane == 31)
             gtile[G] = incl * NT;
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // the peer's barriers are initialised before any multicast lands
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
 
-    const int T = GROUPED ? gtile[p.G] : static_cast<int>(((M + BM - 1) / BM) * NT);
-    const int MT = static_cast<int>((M + BM - 1) / BM);
+    const int MT = static_cast<int>((M + C::TILE_M - 1) / C::TILE_M);
+    const int T = GROUPED ? gtile[p.G] : MT * NT;
 
     auto tile_of = [&](int t) -> Tile {
         Tile ti;
+        int row0, rend;
         if (!GROUPED) {
             const int mt = t % MT, nt = t / MT;
-            ti.row0 = mt * BM;
-            ti.row_end = ti.row0 + BM < M ? ti.row0 + BM : static_cast<int>(M);
+            row0 = mt * C::TILE_M;
+            rend = static_cast<int>(M);
             ti.n0 = nt * BN;
             ti.brow0 = ti.n0;
             ti.sb_base = 0;
@@ -196,15 +241,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int g = lo;
             const int local = t - gtile[g];
-            const int mtg = static_cast<int>((goff[g + 1] - goff[g] + BM - 1) / BM);
+            const int mtg = static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
             const int nt = local / mtg, mt = local - nt * mtg;
-            const int gend = static_cast<int>(goff[g + 1]);
-            ti.row0 = static_cast<int>(goff[g]) + mt * BM;
-            ti.row_end = ti.row0 + BM < gend ? ti.row0 + BM : gend;
+            row0 = goff[g] + mt * C::TILE_M;
+            rend = goff[g + 1];
             ti.n0 = nt * BN;
             ti.brow0 = g * static_cast<int>(N) + ti.n0;
             ti.sb_base = static_cast<int64_t>(g) * p.sb_group_stride;
         }
+        ti.row0 = row0 + static_cast<int>(rank) * 128;
+        ti.row_end = ti.row0 + 128 < rend ? ti.row0 + 128 : rend;
+        ti.brow0 += static_cast<int>(rank) * C::B_ROWS;
         return ti;
     };
 
@@ -215,63 +262,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
             uint32_t it = 0;
-            for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            for (int t = unit; t < T; t += nunits) {
                 const Tile ti = tile_of(t);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(bar(BAR_EMPTY + s), ph ^ 1, ctl, 0x0100 | s))
+                    if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, ctl, 0x0100 | s))
                         goto producer_done;
-                    mbar_arrive_expect_tx(bar(BAR_FULL + s), A_BYTES + B_BYTES);
-                    tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, bar(BAR_FULL + s), kb * BK, ti.row0);
-                    tma_load_2d(smem_u32(smB + s * B_BYTES), &tmB, bar(BAR_FULL + s), kb * BK, ti.brow0);
+                    mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::STAGE_BYTES);
+                    tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, bar(C::BAR_FULL + s), kb * BK, ti.row0);
+                    if (PAIR)
+                        tma_load_2d_mc(smem_u32(smB + s * C::B_BYTES + rank * (C::B_ROWS * BK)), &tmB,
+                                       bar(C::BAR_FULL + s), kb * BK, ti.brow0, 0x3);
+                    else
+                        tma_load_2d(smem_u32(smB + s * C::B_BYTES), &tmB, bar(C::BAR_FULL + s), kb * BK, ti.brow0);
                 }
             }
         producer_done:
             for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-                mbar_wait_drain(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1, p.timeout_ns);
+                mbar_wait_drain(bar(C::BAR_FULL + j % STAGES), (j / STAGES) & 1, p.timeout_ns);
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------------- MMA issuer
-            const uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            const uint32_t idesc = idesc_e4m3_f32(128, BN);
             uint32_t it = 0;
-            for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            for (int t = unit; t < T; t += nunits) {
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     const uint32_t buf = it & 1, tph = (it >> 1) & 1;
-                    if (!mbar_wait(bar(BAR_TEMPTY + buf), tph ^ 1, ctl, 0x0200 | buf))
+                    if (!mbar_wait(bar(C::BAR_TEMPTY + buf), tph ^ 1, ctl, 0x0200 | buf))
                         goto mma_done;
-                    if (!mbar_wait(bar(BAR_FULL + s), ph, ctl, 0x0210 | s))
+                    if (!mbar_wait(bar(C::BAR_FULL + s), ph, ctl, 0x0210 | s))
                         goto mma_done;
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smA + s * A_BYTES);
-                    const uint32_t b0 = smem_u32(smB + s * B_BYTES);
+                    const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
                     const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
                         umma_e4m3(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
                                   k > 0 ? 1u : 0u);
-                    umma_commit(bar(BAR_EMPTY + s));
-                    umma_commit(bar(BAR_TFULL + buf));
+                    if (PAIR)
+                        umma_commit_mc(bar(C::BAR_EMPTY + s), 0x3);   // release the stage in both CTAs
+                    else
+                        umma_commit(bar(C::BAR_EMPTY + s));
+                    umma_commit(bar(C::BAR_TFULL + buf));
                 }
             }
         mma_done:
-            umma_commit(bar(BAR_DRAIN));
-            mbar_wait_drain(bar(BAR_DRAIN), 0, p.timeout_ns);
+            umma_commit(bar(C::BAR_DRAIN));
+            mbar_wait_drain(bar(C::BAR_DRAIN), 0, p.timeout_ns);
         } else if (warp == 2) {
             // ---------------------------------------------------------- scale loader
             uint32_t it = 0;
-            for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            for (int t = unit; t < T; t += nunits) {
                 const Tile ti = tile_of(t);
                 const float *sbg = p.sB + ti.sb_base;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t j = it % SSLOTS, ph = (it / SSLOTS) & 1;
-                    if (!mbar_wait(bar(BAR_SEMPTY + j), ph ^ 1, ctl, 0x0300 | j))
+                    if (!mbar_wait(bar(C::BAR_SEMPTY + j), ph ^ 1, ctl, 0x0300 | j))
                         goto scale_done;
                     const float *sa_row = p.sA + static_cast<int64_t>(kb) * p.ldsa;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int r = ti.row0 + lane + 32 * i;
                         const bool ok = r < ti.row_end;
-                        cp_async_4(smem_u32(ssa + j * BM + lane + 32 * i), ok ? sa_row + r : p.sA, ok ? 4u : 0u);
+                        cp_async_4(smem_u32(ssa + j * 128 + lane + 32 * i), ok ? sa_row + r : p.sA, ok ? 4u : 0u);
                     }
                     if (SCALE_B == kScaleRowKN) {
                         const float *sb_row = sbg + static_cast<int64_t>(kb) * p.ldsb;
@@ -288,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                     : sbg + static_cast<int64_t>(kb) * p.ldsb + nb;
                         cp_async_4(smem_u32(ssb + j * BN + lane), ok ? src : p.sB, ok ? 4u : 0u);
                     }
-                    cp_async_arrive_noinc(bar(BAR_SFULL + j));
+                    cp_async_arrive_noinc(bar(C::BAR_SFULL + j));
                 }
             }
         scale_done:
@@ -302,10 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tm_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        for (int t = unit; t < T && ok; t += nunits) {
             const Tile ti = tile_of(t);
-            // decided before the K loop: keeps the tile bounds out of the loop's live registers
-            const bool store_ok = (ti.row0 + row_in < ti.row_end) && (ti.n0 + half * 128 < N);
             unsigned long long acc[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i)
@@ -313,75 +365,124 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const uint32_t j = it % SSLOTS, sph = (it / SSLOTS) & 1;
                 const uint32_t buf = it & 1, tph = (it >> 1) & 1;
-                if (!mbar_wait(bar(BAR_SFULL + j), sph, ctl, 0x0400 | j) ||
-                    !mbar_wait(bar(BAR_TFULL + buf), tph, ctl, 0x0410 | buf)) {
+                if (!mbar_wait(bar(C::BAR_SFULL + j), sph, ctl, 0x0400 | j) ||
+                    !mbar_wait(bar(C::BAR_TFULL + buf), tph, ctl, 0x0410 | buf)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float sa = ssa[j * BM + row_in];
+                const float sa = ssa[j * 128 + row_in];
                 const unsigned long long sa2 = pack2(sa, sa);
                 float sc = 0.0f;
                 if (SCALE_B != kScaleRowKN)
                     sc = sa * ssb[j * BN + half];
                 const unsigned long long sc2 = pack2(sc, sc);
+                const float *sbcol = ssb + j * BN + half * 128;
                 const uint32_t taddr = tmem_base + tm_lane + buf * BN + half * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    MPQ_TMEM_LD32(taddr + c * 32, v);
-                    MPQ_TMEM_WAIT_LD32(v);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const unsigned long long pv =
-                            (static_cast<unsigned long long>(v[2 * q + 1]) << 32) | v[2 * q];
-                        if (SCALE_B == kScaleRowKN) {
-                            const unsigned long long sb2 = *reinterpret_cast<const unsigned long long *>(
-                                ssb + j * BN + half * 128 + c * 32 + 2 * q);
-                            acc[c * 16 + q] = ffma2(fmul2(pv, sb2), sa2, acc[c * 16 + q]);
-                        } else {
-                            acc[c * 16 + q] = ffma2(pv, sc2, acc[c * 16 + q]);
-                        }
-                    }
-                }
+                // two TMEM loads in flight: 0,1 | 2 while promoting 0 | 3 while promoting 1
+                uint32_t va[32], vb[32];
+                MPQ_TMEM_LD32(taddr, va);
+                MPQ_TMEM_LD32(taddr + 32, vb);
+                MPQ_TMEM_WAIT_LD32(va);
+                MPQ_TMEM_WAIT_LD32(vb);
+                promote_chunk<SCALE_B>(acc, va, 0, sc2, sa2, sbcol);
+                MPQ_TMEM_LD32(taddr + 64, va);
+                promote_chunk<SCALE_B>(acc, vb, 1, sc2, sa2, sbcol);
+                MPQ_TMEM_LD32(taddr + 96, vb);
+                MPQ_TMEM_WAIT_LD32(va);
+                promote_chunk<SCALE_B>(acc, va, 2, sc2, sa2, sbcol);
+                MPQ_TMEM_WAIT_LD32(vb);
+                promote_chunk<SCALE_B>(acc, vb, 3, sc2, sa2, sbcol);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(BAR_TEMPTY + buf));
-                    mbar_arrive(bar(BAR_SEMPTY + j));
+                    mbar_arrive(bar(C::BAR_TEMPTY + buf));
+                    mbar_arrive(bar(C::BAR_SEMPTY + j));
                 }
             }
             if (!ok)
                 break;
-            if (store_ok) {
-                const int64_t m = ti.row0 + row_in;
-                const int64_t n = ti.n0 + half * 128;
-                if (OUT_F32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + m * p.ldc + n);
+            // Output: rows [ti.row0 + 32 quad, +32), columns [ti.n0 + 128 half, +128).  A warp
+            // whose 32 rows all belong to this tile stages 64-byte row pieces in its swizzled
+            // 2 KB buffer and writes them with TMA stores (clipped at the tensor bounds);
+            // a warp on a ragged expert boundary stores its valid rows directly.
+            const int wrow0 = ti.row0 + quad * 32;
+            const int ncol0 = ti.n0 + half * 128;
+            if (ncol0 < N) {
+                const bool whole = GROUPED ? (wrow0 + 32 <= ti.row_end) : true;
+                if (whole) {
+                    uint8_t *stg = smO + ew * STAGE_OUT;
+                    const uint32_t stg_u32 = smem_u32(stg);
+                    constexpr int COLS = OUT_F32 ? 16 : 32;          // columns per 64-byte row piece
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        dst[i] = make_float4(lo_of(acc[2 * i]), hi_of(acc[2 * i]), lo_of(acc[2 * i + 1]),
-                                             hi_of(acc[2 * i + 1]));
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n);
+                    for (int ch = 0; ch < 128 / COLS; ++ch) {
+                        if (lane == 0)
+                            bulk_wait_read0();                          // previous piece has left smem
+                        __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        uint32_t w[4];
+                        for (int j = 0; j < 4; ++j) {                   // four 16-byte pieces of the row
+                            uint4 w;
+                            if (OUT_F32) {
+                                const int a0 = (ch * 16 + j * 4) / 2;   // acc index of columns ch*16+4j..+3
+                                w = make_uint4(__float_as_uint(lo_of(acc[a0])), __float_as_uint(hi_of(acc[a0])),
+                                               __float_as_uint(lo_of(acc[a0 + 1])), __float_as_uint(hi_of(acc[a0 + 1])));
+                            } else {
+                                const int a0 = (ch * 32 + j * 8) / 2;   // acc index of columns ch*32+8j..+7
+                                uint32_t h[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __nv_bfloat162 b2 =
-                                __floats2bfloat162_rn(lo_of(acc[4 * i + k]), hi_of(acc[4 * i + k]));
-                            w[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                                for (int k = 0; k < 4; ++k) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo_of(acc[a0 + k]), hi_of(acc[a0 + k]));
+                                    h[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                                }
+                                w = make_uint4(h[0], h[1], h[2], h[3]);
+                            }
+                            // 64-byte swizzle: 16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3)
+                            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg_u32 + off), "r"(w.x),
+                                         "r"(w.y), "r"(w.z), "r"(w.w)
+                                         : "memory");
                         }
-                        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, stg_u32, ncol0 + ch * COLS, wrow0);
+                            bulk_commit();
+                        }
+                    }
+                } else if (wrow0 + lane < ti.row_end) {
+                    const int64_t m = wrow0 + lane;
+                    const int64_t n = ncol0;
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + m * p.ldc + n);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            dst[i] = make_float4(lo_of(acc[2 * i]), hi_of(acc[2 * i]), lo_of(acc[2 * i + 1]),
+                                                 hi_of(acc[2 * i + 1]));
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.C) + m * p.ldc + n);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __nv_bfloat162 b2 =
+                                    __floats2bfloat162_rn(lo_of(acc[4 * i + k]), hi_of(acc[4 * i + k]));
+                                w[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
             }
         }
+        if (lane == 0)
+            bulk_wait0();   // every TMA store of this warp has completed
     }
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // no multicast into this CTA or commit from the peer is pending
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
@@ -405,12 +506,12 @@ __global__ void wait_selftest_kernel(int *status, uint64_t timeout_ns)
     }
 }
 
-template <int SB, bool F32, bool GR>
-cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, int grid,
-                       cudaStream_t st)
+template <int SB, bool F32, bool GR, bool PAIR>
+cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
+                       int grid, cudaStream_t st)
 {
-    auto kern = gemm_kernel<SB, F32, GR>;
-    const size_t smem = smem_bytes(GR);
+    auto kern = gemm_kernel<SB, F32, GR, PAIR>;
+    const size_t smem = smem_bytes<PAIR>(GR);
     static bool configured = false;  // one attribute call per instantiation and process
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -419,39 +520,63 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const Gem
             return e;
         configured = true;
     }
-    kern<<<grid, kThreads, smem, st>>>(tmA, tmB, a);
-    return cudaGetLastError();
+    if (!PAIR) {
+        kern<<<grid, kThreads, smem, st>>>(tmA, tmB, tmC, a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
 }
 
 } // namespace
 
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, int scale_b,
-                        bool out_fp32, int num_sms, cudaStream_t st)
+int gemm_b_box_rows(bool pair) { return pair ? Cfg<true>::B_ROWS : Cfg<false>::B_ROWS; }
+
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
+                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st)
 {
     const bool grouped = a.offsets != nullptr;
     if (grouped && a.G > kMaxGroups)
         return cudaErrorInvalidValue;
+    const int tile_m = pair ? 256 : 128;
     int64_t tiles;
-    if (grouped) {
-        // upper bound: every expert may add one partial m-tile
-        tiles = ((a.M + BM - 1) / BM + a.G) * ((a.N + BN - 1) / BN);
-    } else {
-        tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-    }
+    if (grouped)  // upper bound: every expert may add one partial m-tile
+        tiles = ((a.M + tile_m - 1) / tile_m + a.G) * ((a.N + BN - 1) / BN);
+    else
+        tiles = ((a.M + tile_m - 1) / tile_m) * ((a.N + BN - 1) / BN);
     if (tiles <= 0)
         return cudaSuccess;
-    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-#define MPQ_G(SB, F32, GR)                                                     \
-    if (scale_b == SB && out_fp32 == F32 && grouped == GR)                     \
-        return launch_one<SB, F32, GR>(tmA, tmB, a, grid, st);
-    MPQ_G(kScaleBlockNK, false, false)
-    MPQ_G(kScaleBlockNK, true, false)
-    MPQ_G(kScaleBlockKN, false, false)
-    MPQ_G(kScaleBlockKN, true, false)
-    MPQ_G(kScaleRowKN, false, false)
-    MPQ_G(kScaleRowKN, true, false)
-    MPQ_G(kScaleBlockNK, false, true)
-    MPQ_G(kScaleBlockNK, true, true)
+    int grid;
+    if (pair) {
+        const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+        grid = static_cast<int>(2 * (pairs < 1 ? 1 : pairs));
+    } else {
+        grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    }
+#define MPQ_G(SB, F32, GR, PR)                                                             \
+    if (scale_b == SB && out_fp32 == F32 && grouped == GR && pair == PR)                   \
+        return launch_one<SB, F32, GR, PR>(tmA, tmB, tmC, a, grid, st);
+#define MPQ_G2(SB, F32, GR) MPQ_G(SB, F32, GR, true) MPQ_G(SB, F32, GR, false)
+    MPQ_G2(kScaleBlockNK, false, false)
+    MPQ_G2(kScaleBlockNK, true, false)
+    MPQ_G2(kScaleBlockKN, false, false)
+    MPQ_G2(kScaleBlockKN, true, false)
+    MPQ_G2(kScaleRowKN, false, false)
+    MPQ_G2(kScaleRowKN, true, false)
+    MPQ_G2(kScaleBlockNK, false, true)
+    MPQ_G2(kScaleBlockNK, true, true)
+#undef MPQ_G2
 #undef MPQ_G
     return cudaErrorInvalidValue;
 }

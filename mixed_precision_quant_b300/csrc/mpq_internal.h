@@ -49,8 +49,12 @@ struct GemmArgs {
 // Block-scaled FP8 GEMM on tcgen05: C[M,N] = sum over 128-wide K slices of
 // (A_slice B_slice^T) * sA * sB, promoted into FP32 after every slice.
 // tmA covers A [rows, K] E4M3, tmB covers B [rows, K] E4M3 (both K-major, 128B swizzle).
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, int scale_b,
-                        bool out_fp32, int num_sms, cudaStream_t st);
+// `pair`: 2-CTA clusters sharing B through multicast; each CTA then loads B in boxes of
+// gemm_b_box_rows(true) = 128 rows, else 256.
+// tmC: output view [rows, N] (BF16 or FP32) with box 64 bytes x 32 rows, 64-byte swizzle.
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
+                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st);
+int gemm_b_box_rows(bool pair);
 
 // Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);

@@ -24,6 +24,14 @@ def mpq():
     return m
 
 
+@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+def tiles(request, mpq):
+    """Run the test with 256x256 tiles on SM pairs and with 128x256 tiles on single SMs."""
+    mpq.mpq_set_gemm_cta_pair(request.param)
+    yield request.param
+    mpq.mpq_set_gemm_cta_pair(True)
+
+
 def _bf16(shape, std, seed, outliers=0.0):
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(shape, generator=g) * std
@@ -46,7 +54,7 @@ def _out_host(C):
 @pytest.mark.parametrize("M,N,K", [(300, 512, 1024), (128, 256, 128), (1, 256, 256), (77, 384, 640),
                                    (129, 128, 8192)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
-def test_fprop_oracle_operands(mpq, M, N, K, out):
+def test_fprop_oracle_operands(mpq, tiles, M, N, K, out):
     a = _bf16((M, K), 1.0, M * 7 + K, outliers=0.01)
     w = _bf16((N, K), 0.02, N * 13 + K)
     qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
@@ -57,7 +65,7 @@ def test_fprop_oracle_operands(mpq, M, N, K, out):
     assert_gemm_close(_out_host(C), ref, absref, f"fprop {M}x{N}x{K} {out}")
 
 
-def test_fprop_small_integers_exact(mpq):
+def test_fprop_small_integers_exact(mpq, tiles):
     """Codes of small integers with unit scales: every partial and sum is an exact
     integer below 2^24, so the FP32 output must equal the integer matmul exactly."""
     g = np.random.default_rng(3)
@@ -89,7 +97,7 @@ def test_fprop_tiny_config_end_to_end(mpq):
 # --------------------------------------------------------------------- Dgrad
 
 @pytest.mark.parametrize("T,Nout,Kin", [(256, 512, 384), (200, 256, 256)])
-def test_dgrad_pow2(mpq, T, Nout, Kin):
+def test_dgrad_pow2(mpq, tiles, T, Nout, Kin):
     """dX[T, Kin] = dY[T, Nout] . W_lin[Nout, Kin]: A = dY (1x128, power-of-2 scales),
     B = transposed weight codes [Kin, Nout] with the weight's block scales."""
     g = torch.Generator().manual_seed(T)
@@ -105,7 +113,7 @@ def test_dgrad_pow2(mpq, T, Nout, Kin):
 # --------------------------------------------------------------------- Wgrad
 
 @pytest.mark.parametrize("T,Kin,Nout", [(512, 384, 256), (256, 128, 512)])
-def test_wgrad(mpq, T, Kin, Nout):
+def test_wgrad(mpq, tiles, T, Kin, Nout):
     """dW[Kin, Nout] = X^T dY: both operands quantized in 128x1 tiles along tokens."""
     g = torch.Generator().manual_seed(T + Kin)
     x = _bf16((T, Kin), 1.0, T)
@@ -201,4 +209,4 @@ def test_bounded_wait_reports_timeout_and_context_survives(mpq):
     st, where = mpq.mpq_check_device_status()
     assert st == 6 and where == 0x7F01
     assert mpq.mpq_check_device_status()[0] == 0  # cleared on read
-    test_fprop_small_integers_exact(mpq)
+    test_fprop_small_integers_exact(mpq, True)

@@ -18,6 +18,14 @@ def mpq():
     return m
 
 
+@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+def tiles(request, mpq):
+    """Run the test with 256x256 tiles on SM pairs and with 128x256 tiles on single SMs."""
+    mpq.mpq_set_gemm_cta_pair(request.param)
+    yield request.param
+    mpq.mpq_set_gemm_cta_pair(True)
+
+
 def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -38,7 +46,7 @@ def _experts(G, N, K, seed):
     ([128, 128], 0, 0),
     ([1] * 40, 3, 0),
 ])
-def test_grouped_small(mpq, counts, lead, trail):
+def test_grouped_small(mpq, tiles, counts, lead, trail):
     G, N, K = len(counts), 256, 384
     off = np.concatenate([[0], np.cumsum(counts)]) + lead
     M = int(off[-1]) + trail
@@ -57,7 +65,7 @@ def test_grouped_small(mpq, counts, lead, trail):
     assert np.all(got[~rows] == 12345.0), "rows outside every expert were written"
 
 
-def test_grouped_equals_single_gemms(mpq):
+def test_grouped_equals_single_gemms(mpq, tiles):
     """Cross-path invariant: each expert's rows equal a single-GEMM call, bit for bit."""
     counts = [70, 300, 0, 129]
     G, N, K = len(counts), 384, 256
