@@ -60,20 +60,36 @@ mpq_status encode_operand(CUtensorMap *m, const uint8_t *ptr, int64_t rows, int6
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
-// 2-D BF16 source view [rows, cols] (cols contiguous), box 128 columns x box_rows, no
-// swizzle, out-of-bounds rows read as zero.
-mpq_status encode_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows)
+// 2-D BF16 source view [rows, cols] (cols contiguous), boxes of 128 rows x 64 columns
+// (128 bytes) with 128-byte swizzle; out-of-bounds rows read as zero.
+mpq_status encode_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
         return MPQ_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t box[2] = {64, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
+}
+
+// E4M3 code view [rows, cols] (cols contiguous), boxes of 128 rows x 128 bytes with 128-byte
+// swizzle (the quantizers' staging layout); stores are clipped at the tensor bounds.
+mpq_status encode_codes(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return MPQ_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
@@ -217,13 +233,19 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
     a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
     a.qT = qT; a.ldqT = ldqT; a.sT = sT; a.ldsT = ldsT;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    CUtensorMap tm;
-    mpq_status e = encode_bf16(&tm, x, rows, cols, ldx, qT == nullptr ? 64 : 128);
+    CUtensorMap tmx, tmq, tmqT;
+    mpq_status e = encode_bf16(&tmx, x, rows, cols, ldx);
+    if (e == MPQ_OK && q != nullptr)
+        e = encode_codes(&tmq, q, rows, cols, ldq);
+    if (e == MPQ_OK && qT != nullptr)
+        e = encode_codes(&tmqT, qT, cols, rows, ldqT);
     if (e != MPQ_OK)
         return e;
+    if (q == nullptr)
+        tmq = tmqT;   // unused by the kernel
     if (qT == nullptr)
-        return from_cuda(mpq::launch_quant_rows(tm, a, pow2, h->num_sms, st));
-    return from_cuda(mpq::launch_quant_dual(tm, a, pow2, h->num_sms, st));
+        return from_cuda(mpq::launch_quant_rows(tmx, tmq, a, pow2, h->num_sms, st));
+    return from_cuda(mpq::launch_quant_dual(tmx, tmq, tmqT, a, pow2, h->num_sms, st));
 }
 
 mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, int64_t cols, int64_t ldw,
@@ -249,11 +271,17 @@ mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, in
     a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
     a.qT = qT; a.ldqT = ldqT;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    CUtensorMap tm;
-    mpq_status e = encode_bf16(&tm, w, rows, cols, ldw, 128);
+    CUtensorMap tmx, tmq, tmqT;
+    mpq_status e = encode_bf16(&tmx, w, rows, cols, ldw);
+    if (e == MPQ_OK)
+        e = encode_codes(&tmq, q, rows, cols, ldq);
+    if (e == MPQ_OK && qT != nullptr)
+        e = encode_codes(&tmqT, qT, cols, rows, ldqT);
     if (e != MPQ_OK)
         return e;
-    return from_cuda(mpq::launch_quant_block(tm, a, (flags & MPQ_POW2) != 0, h->num_sms,
+    if (qT == nullptr)
+        tmqT = tmq;   // unused by the kernel
+    return from_cuda(mpq::launch_quant_block(tmx, tmq, tmqT, a, (flags & MPQ_POW2) != 0, h->num_sms,
                                              static_cast<cudaStream_t>(stream)));
 }
 

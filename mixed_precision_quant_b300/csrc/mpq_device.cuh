@@ -383,68 +383,79 @@ __device__ __forceinline__ int pow2_exponent(float amax)
 
 struct GroupScale {
     float s;     // the stored scale
-    float rlo;   // multipliers bracketing the quotient (see e4m3_pair), or the exact
-    float rhi;   //   multiplier 2^-e when the scale is a power of two
-    int mode;    // 0: bracket, 1: exact multiplier, 2: divide
+    float r;     // RN(1 / s) (mode 0), or the exact reciprocal 2^-e of a power-of-2 scale (mode 1)
+    int mode;    // 0: product plus one correction step, 1: exact product, 2: IEEE division
 };
+
+// Scales below this use the IEEE division: the correction step needs an exact remainder
+// (see e4m3_pair), which holds when ulp(s) * 2^-33 >= 2^-149, i.e. s >= 2^-93.
+constexpr float kMinCorrectedScale = 0x1p-80f;
 
 // Scale of a group from its max-abs value.
 __device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
 {
     GroupScale g;
     if (amax == 0.0f) {
-        g.s = 1.0f; g.rlo = 1.0f; g.rhi = 1.0f; g.mode = 1;
+        g.s = 1.0f; g.r = 1.0f; g.mode = 1;
         return g;
     }
     if (pow2) {
         const int e = pow2_exponent(amax);
         g.s = exp2_int(e);
-        if (e >= -126) { g.rlo = g.rhi = exp2_int(-e); g.mode = 1; }
-        else { g.rlo = g.rhi = 0.0f; g.mode = 2; }
+        if (e >= -126) { g.r = exp2_int(-e); g.mode = 1; }
+        else { g.r = 0.0f; g.mode = 2; }
         return g;
     }
     g.s = __fdiv_rn(amax, 448.0f);
-    if (g.s < 1.17549435e-38f) {
-        g.rlo = g.rhi = 0.0f; g.mode = 2;
+    if (g.s < kMinCorrectedScale) {
+        g.r = 0.0f; g.mode = 2;
         return g;
     }
-    const float r = __frcp_rn(g.s);
-    g.rlo = __fmul_rn(r, 1.0f - 0x1p-21f);
-    g.rhi = __fmul_rn(r, 1.0f + 0x1p-21f);
+    g.r = __frcp_rn(g.s);
     g.mode = 0;
     return g;
 }
 
-// IEEE binary32 division, kept out of line: it only runs for the rare values the bracket
-// cannot decide and for subnormal scales.
+// IEEE binary32 division, kept out of line: it only runs for groups whose scale lies below
+// kMinCorrectedScale (max-abs value below about 2^-71).
 static __device__ __noinline__ float exact_quotient(float x, float s) { return __fdiv_rn(x, s); }
 
-// E4M3 codes of the binary32 quotients x0 / s and x1 / s (each correctly rounded to
-// binary32, then rounded to nearest even E4M3 with saturation); byte 0 = x0.
+// Correctly rounded binary32 quotients x / s of a pair, negated, for mode 0.
 //
-// Method (bracketing by monotonicity): with r = RN(1/s), the products
-// lo = RN(x * RN(r (1 - 2^-21))) and hi = RN(x * RN(r (1 + 2^-21))) satisfy
-// |lo| <= |RN(x / s)| <= |hi|, because the exact products differ from x / s by a relative
-// factor in (1 - 2^-21 - 2^-22, 1 - 2^-22) and (1 + 2^-22, 1 + 2^-21 + 2^-22) and
-// rounding to nearest is monotone.  Rounding binary32 to E4M3 is monotone too, so when
-// lo and hi give the same code, every value between them -- RN(x / s) included -- gives
-// that code.  Otherwise (a quotient within about 3 binary32 ulps of an E4M3 rounding
-// boundary) the quotient is recomputed with the IEEE division.  For power-of-2 scales
+// Method: the correction step of Markstein's division (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
+// 1990).  With r = RN(1/s) and q0 = RN(x r) -- within one ulp of x / s -- the remainder
+// x - q0 s is a binary32 number, so one fused multiply-add computes it exactly, and
+// RN(q0 + (x - q0 s) r) = RN(x / s).  The remainder is exact when it cannot fall below the
+// binary32 subnormal grid: for |q0| >= 2^-11 that needs s >= 2^-93 (kMinCorrectedScale keeps
+// a margin), and a quotient below 2^-11 gives the code 0 whatever its last bits.
+//
+// The steps run on -r: nq0 = x (-r) = -q0, e = nq0 s + x = x - q0 s, t = e (-r) + nq0 =
+// -RN(x / s).  Negated this way, t also carries the sign of x when x is a signed zero
+// (t = -0 for x = +0 and +0 for x = -0), so the E4M3 code of x / s is the code of t with
+// its sign bit flipped -- rounding to nearest even and saturation are symmetric in sign.
+__device__ __forceinline__ unsigned long long neg_quotient2(unsigned long long x, unsigned long long nr,
+                                                            unsigned long long s)
+{
+    const unsigned long long nq0 = fmul2(x, nr);
+    const unsigned long long e = ffma2(nq0, s, x);
+    return ffma2(e, nr, nq0);
+}
+
+// E4M3 codes of the correctly rounded binary32 quotients x0 / s and x1 / s, each then
+// rounded to nearest even E4M3 with saturation; byte 0 = x0.  For power-of-2 scales
 // x * 2^-e is the quotient itself (mode 1).
 __device__ __forceinline__ uint32_t e4m3_pair(float x0, float x1, const GroupScale &g)
 {
     if (g.mode == 2)
         return e4m3x2(exact_quotient(x0, g.s), exact_quotient(x1, g.s));
     const unsigned long long x = pack2(x0, x1);
-    const unsigned long long lo = fmul2(x, pack2(g.rlo, g.rlo));
-    if (g.mode == 1)
-        return e4m3x2(lo_of(lo), hi_of(lo));
-    const unsigned long long hi = fmul2(x, pack2(g.rhi, g.rhi));
-    const uint32_t clo = e4m3x2(lo_of(lo), hi_of(lo));
-    const uint32_t chi = e4m3x2(lo_of(hi), hi_of(hi));
-    if (__builtin_expect(clo == chi, 1))
-        return clo;
-    return e4m3x2(exact_quotient(x0, g.s), exact_quotient(x1, g.s));
+    if (g.mode == 1) {
+        const unsigned long long p = fmul2(x, pack2(g.r, g.r));
+        return e4m3x2(lo_of(p), hi_of(p));
+    }
+    const unsigned long long t = neg_quotient2(x, pack2(-g.r, -g.r), pack2(g.s, g.s));
+    return e4m3x2(lo_of(t), hi_of(t)) ^ 0x8080u;
 }
 
 // Single-value form (code in the low byte).

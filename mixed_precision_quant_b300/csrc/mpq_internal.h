@@ -7,16 +7,16 @@
 
 namespace mpq {
 
-// Quantizer arguments.  The BF16 source is read through a 2-D TMA view (tensor map)
-// encoded by the caller: [rows, cols] with box 128 columns x (64 rows for the row
-// quantizer, 128 rows for the dual and block quantizers).
+// Quantizer arguments.  Tensors are read and written through TMA views encoded by the
+// caller: the BF16 source [rows, cols] in 128-row x 64-column boxes, and the E4M3 outputs
+// q [rows, cols] / qT [cols, rows] in 128 x 128-byte boxes, all with 128-byte swizzle.
 struct QuantArgs {
     int64_t rows, cols;
-    uint8_t *q;         // row-wise (or block) codes [rows, cols], ldq
+    uint8_t *q;         // row-wise (or block) codes [rows, cols] (may be null for the dual kernel)
     int64_t ldq;
     float *s;           // row-wise scales [cols/128][lds] or block scales [rows/128][lds]
     int64_t lds;
-    uint8_t *qT;        // transposed codes [cols, rows], ldqT (optional)
+    uint8_t *qT;        // transposed codes [cols, rows] (optional)
     int64_t ldqT;
     float *sT;          // column-group scales [rows/128][ldsT]
     int64_t ldsT;
@@ -24,9 +24,12 @@ struct QuantArgs {
     uint64_t timeout_ns;
 };
 
-cudaError_t launch_quant_rows(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
-cudaError_t launch_quant_dual(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
-cudaError_t launch_quant_block(const CUtensorMap &tmx, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
+                              int num_sms, cudaStream_t st);
+cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
+                              const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
+                               const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st);
 
 // Which B-side scale layout the GEMM reads (see fp8_gemm_blockscaled in mpq.h).
 enum ScaleB : int { kScaleBlockNK = 0, kScaleBlockKN = 1, kScaleRowKN = 2 };

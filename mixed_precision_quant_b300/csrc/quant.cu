@@ -10,16 +10,28 @@
 //   * 128x1 column groups (one scale per column per 128 rows), written transposed,
 //   * 128x128 blocks (one scale per block), optionally also written transposed.
 //
-// All three kernels are persistent and warp-specialised: one producer warp streams BF16
-// tiles into a shared-memory ring with 2-D TMA loads (completion counted on mbarriers),
-// eight consumer warps reduce group max-abs values with warp shuffles, convert with the
-// exact scale arithmetic of mpq_device.cuh and write E4M3 codes with coalesced stores
-// (transposed codes are staged through shared memory).  Every wait is bounded.
+// Design.  All three kernels are persistent and warp-specialised around tiles of
+// 256 rows x 128 columns of BF16 (64 KB):
+//   * one producer warp loads a tile as four 128-row x 64-column TMA boxes with 128-byte
+//     swizzle into a shared-memory ring (completion counted on mbarriers);
+//   * eight consumer warps own one row each per thread (row groups) or one column group
+//     each per thread (column groups): a thread reads its 128 values with conflict-free
+//     16-byte (or 2-byte) shared loads, reduces the max-abs itself, derives the scale once
+//     and converts with the exact arithmetic of mpq_device.cuh;
+//   * codes are written into 128-byte-swizzled staging tiles, one per warpgroup, and
+//     leave with TMA bulk-tensor stores (coalesced, clipped at the tensor bounds).
+// Every wait is bounded.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
 
 namespace mpq {
 namespace {
+
+constexpr int kConsumers = 8;                       // consumer warps per CTA
+constexpr int kQThreads = 32 * (kConsumers + 1);    // + one producer warp
+constexpr int kTileRows = 256;                      // rows per tile
+constexpr uint32_t kBox = 128 * 128;                // one 128-row x 128-byte box (16 KB)
+constexpr uint32_t kTile = 4 * kBox;                // 256 x 128 BF16 = 64 KB
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr)
 {
@@ -35,10 +47,26 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
     return v;
 }
 
-// Barrier among the consumer warps only (the producer warp does not take part), on an
-// mbarrier so that the wait is bounded: lane 0 of each warp arrives after the warp's
-// own shared-memory writes, every lane waits for the phase.  Returns false on abort.
-__device__ __forceinline__ bool consumers_sync(uint32_t bar, uint32_t &k, const WaitCtl &ctl, int tag)
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Byte offset of 16-byte chunk j of row r in a 128-row box with 128-byte swizzle (the
+// layout TMA writes and reads with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint32_t sw128(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
+
+// Bounded barrier among the four warps of one warpgroup (the mbarrier counts 4 warps):
+// lane 0 of each warp arrives after the warp's own writes, every lane waits.
+__device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t &k, const WaitCtl &ctl, int tag)
 {
     __syncwarp();
     if ((threadIdx.x & 31) == 0)
@@ -48,444 +76,434 @@ __device__ __forceinline__ bool consumers_sync(uint32_t bar, uint32_t &k, const 
     return ok;
 }
 
-// max |x| over eight BF16 values, in packed BF16x2 arithmetic (exact), as binary32.
-__device__ __forceinline__ float amax8(const uint4 &v)
+// max |x| of the BF16 pairs in w[0..N), in packed BF16x2 arithmetic (exact), as binary32.
+template <int N>
+__device__ __forceinline__ float amax_words(const uint32_t (&w)[N])
 {
-    uint32_t m;
-    const uint32_t a0 = v.x & 0x7FFF7FFFu, a1 = v.y & 0x7FFF7FFFu, a2 = v.z & 0x7FFF7FFFu, a3 = v.w & 0x7FFF7FFFu;
-    asm("{\n\t.reg .b32 t0, t1;\n\t"
-        "max.bf16x2 t0, %1, %2;\n\t"
-        "max.bf16x2 t1, %3, %4;\n\t"
-        "max.bf16x2 %0, t0, t1;\n\t}"
-        : "=r"(m) : "r"(a0), "r"(a1), "r"(a2), "r"(a3));
-    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
-}
-
-__device__ __forceinline__ float half_warp_amax(float a)
-{
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    return a;
-}
-
-// Eight BF16 values (one 16-byte chunk) -> eight E4M3 codes (8 bytes, memory order kept).
-__device__ __forceinline__ uint2 codes8(const uint4 &v, const GroupScale &g)
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t c[4];
+    uint32_t m[N];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        c[j] = e4m3_pair(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j])), g);
-    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
-// The group scale owned by lane `src` of the warp.
-__device__ __forceinline__ GroupScale shfl_scale(const GroupScale &g, int src)
-{
-    GroupScale o;
-    o.s = __shfl_sync(0xffffffffu, g.s, src);
-    o.rlo = __shfl_sync(0xffffffffu, g.rlo, src);
-    o.rhi = __shfl_sync(0xffffffffu, g.rhi, src);
-    o.mode = __shfl_sync(0xffffffffu, g.mode, src);
-    return o;
-}
-
-// Row groups held by a warp as row pairs: v[i] holds 8 values of row 2i + (lane >= 16).
-// Lane l (l < 2P) computes the scale of row l once (returned); every row pair then takes
-// its scale from the owner lane by shuffle and converts its values.
-template <int P, bool POW2>
-__device__ __forceinline__ GroupScale row_codes(const uint4 (&v)[P], uint2 (&out)[P])
-{
-    const int lane = threadIdx.x & 31, half = lane >> 4;
-    float my_amax = 0.0f;
+    for (int i = 0; i < N; ++i)
+        m[i] = w[i] & 0x7FFF7FFFu;
 #pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const float a = half_warp_amax(amax8(v[i]));
-        const float other = __shfl_xor_sync(0xffffffffu, a, 16);
-        if ((lane >> 1) == i)
-            my_amax = ((lane & 1) == half) ? a : other;
+    for (int s = N / 2; s > 0; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i)
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[i]), "r"(m[i + s]));
+    return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xFFFF0000u));
+}
+
+// Sixteen BF16 values (8 words, memory order) -> sixteen E4M3 codes (one 16-byte chunk),
+// straight-line for the two common modes so that a thread's conversions overlap.
+__device__ __forceinline__ uint4 codes16(const uint32_t *w, const GroupScale &g)
+{
+    uint32_t c[8];
+    uint32_t flip = 0;
+    if (g.mode == 0) {
+        const unsigned long long nr = pack2(-g.r, -g.r), s2 = pack2(g.s, g.s);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const unsigned long long t =
+                neg_quotient2(pack2(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j]))), nr, s2);
+            c[j] = e4m3x2(lo_of(t), hi_of(t));
+        }
+        flip = 0x80808080u;
+    } else if (g.mode == 1) {
+        const unsigned long long r = pack2(g.r, g.r);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const unsigned long long p =
+                fmul2(pack2(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j]))), r);
+            c[j] = e4m3x2(lo_of(p), hi_of(p));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            c[j] = e4m3_pair(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j])), g);
     }
-    const GroupScale mine = make_group_scale(my_amax, POW2);
-#pragma unroll
-    for (int i = 0; i < P; ++i)
-        out[i] = codes8(v[i], shfl_scale(mine, 2 * i + half));
-    return mine;
+    return make_uint4((c[0] | (c[1] << 16)) ^ flip, (c[2] | (c[3] << 16)) ^ flip, (c[4] | (c[5] << 16)) ^ flip,
+                      (c[6] | (c[7] << 16)) ^ flip);
 }
 
 // ------------------------------------------------------------------ shared layout
 
-constexpr int kConsumers = 8;                       // consumer warps per CTA
-constexpr int kQThreads = 32 * (kConsumers + 1);    // + one producer warp
-constexpr int kQtPitch = 144;                       // bytes per row of a transposed code tile
-
-struct QuantSmem {
-    uint8_t *stage;      // ring of tiles (BF16, rows of 256 bytes)
-    uint64_t *bars;      // full[S], empty[S], consumer barrier
+struct QSmem {
+    uint32_t stage;      // ring of BF16 tiles (64 KB each)
+    uint32_t out_rows;   // 2 x 16 KB row-code staging tiles (one per warpgroup)
+    uint32_t out_cols;   // 2 x 16 KB transposed-code staging tiles (one per warpgroup)
+    uint32_t bars;       // full[S], empty[S], wg[2]
     volatile int *abort;
-    uint8_t *extra;      // kernel-specific scratch (transposed tiles, reductions), 16-byte aligned
+    float *red;          // 8 per-warp partial maxima
 };
 
-// Bytes of the fixed part: ring + barriers + abort flag, before the kernel's extra area.
-template <int STAGES, int TILE_BYTES>
-constexpr size_t ring_bytes() { return 128 + STAGES * TILE_BYTES + (2 * STAGES + 1) * 8 + 24; }
+template <int STAGES, bool COLS>
+constexpr size_t q_smem_bytes() { return 1024 + STAGES * kTile + 2 * kBox + (COLS ? 2 * kBox : 0) + 256; }
 
-template <int STAGES, int TILE_BYTES>
-__device__ __forceinline__ QuantSmem carve(uint8_t *raw)
+template <int STAGES, bool COLS>
+__device__ __forceinline__ QSmem q_carve(uint8_t *raw)
 {
-    QuantSmem s;
-    uint8_t *base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
-    s.stage = base;
-    s.bars = reinterpret_cast<uint64_t *>(base + STAGES * TILE_BYTES);
-    s.abort = reinterpret_cast<volatile int *>(s.bars + 2 * STAGES + 1);
-    s.extra = base + ((STAGES * TILE_BYTES + (2 * STAGES + 1) * 8 + 8 + 15) & ~15);
+    QSmem s;
+    const uint32_t base0 = smem_u32(raw);
+    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
+    s.stage = base0 + pad;
+    s.out_rows = s.stage + STAGES * kTile;
+    s.out_cols = s.out_rows + 2 * kBox;
+    s.bars = s.out_cols + (COLS ? 2 * kBox : 0);
+    uint8_t *tail = raw + pad + STAGES * kTile + 2 * kBox + (COLS ? 2 * kBox : 0);
+    s.abort = reinterpret_cast<volatile int *>(tail + (2 * STAGES + 2) * 8);
+    s.red = reinterpret_cast<float *>(tail + (2 * STAGES + 2) * 8 + 16);
     return s;
 }
 
 template <int STAGES>
-__device__ __forceinline__ void init_ring(const QuantSmem &s)
+__device__ __forceinline__ void q_init(const QSmem &s)
 {
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(smem_u32(s.bars + i), 1);
-            mbar_init(smem_u32(s.bars + STAGES + i), kConsumers);
+            mbar_init(s.bars + 8 * i, 1);
+            mbar_init(s.bars + 8 * (STAGES + i), kConsumers);
         }
-        mbar_init(smem_u32(s.bars + 2 * STAGES), kConsumers);
+        mbar_init(s.bars + 8 * (2 * STAGES), 4);
+        mbar_init(s.bars + 8 * (2 * STAGES + 1), 4);
         *s.abort = 0;
         fence_barrier_init();
     }
     __syncthreads();
 }
 
-// Producer: one lane streams tile `item` (row block, column block) into the ring.
-template <int STAGES, int TILE_ROWS>
-__device__ __forceinline__ void produce(const QuantSmem &s, const CUtensorMap *tm, int64_t items, int64_t ncb,
-                                        const WaitCtl &ctl, uint64_t timeout_ns)
+// Producer: one lane streams tile `item` (256-row block rb, 128-column block cb) into the
+// ring as four boxes; out-of-bounds rows read as zero.
+template <int STAGES>
+__device__ __forceinline__ void q_produce(const QSmem &s, const CUtensorMap *tm, int64_t items, int64_t ncb,
+                                          const WaitCtl &ctl, uint64_t timeout_ns)
 {
-    constexpr uint32_t bytes = TILE_ROWS * 256;
     uint32_t it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
-        if (!mbar_wait(smem_u32(s.bars + STAGES + st), ph ^ 1, ctl, 0x1100 | st))
+        if (!mbar_wait(s.bars + 8 * (STAGES + st), ph ^ 1, ctl, 0x1100 | st))
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
-        mbar_arrive_expect_tx(smem_u32(s.bars + st), bytes);
-        tma_load_2d(smem_u32(s.stage + st * bytes), tm, smem_u32(s.bars + st), static_cast<int32_t>(cb * 128),
-                    static_cast<int32_t>(rb * TILE_ROWS));
+        const uint32_t full = s.bars + 8 * st;
+        mbar_arrive_expect_tx(full, kTile);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            tma_load_2d(s.stage + st * kTile + b * kBox, tm, full, static_cast<int32_t>(cb * 128 + (b & 1) * 64),
+                        static_cast<int32_t>(rb * kTileRows + (b >> 1) * 128));
     }
-    // drain: copies still in flight must land before the CTA exits
     for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(s.bars + j % STAGES), (j / STAGES) & 1))
+        while (!mbar_try_wait(s.bars + 8 * (j % STAGES), (j / STAGES) & 1))
             if (globaltimer_ns() - t0 > timeout_ns)
                 break;
     }
 }
 
+// Row r (0..255) of the tile at `tile`: its 128 values as 64 BF16x2 words, memory order.
+__device__ __forceinline__ void load_row(uint32_t tile, int r, uint32_t (&w)[64])
+{
+    const int rh = r >> 7, rr = r & 127;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = lds_v4(tile + (rh * 2 + ch) * kBox + sw128(rr, j));
+            w[ch * 32 + j * 4 + 0] = v.x;
+            w[ch * 32 + j * 4 + 1] = v.y;
+            w[ch * 32 + j * 4 + 2] = v.z;
+            w[ch * 32 + j * 4 + 3] = v.w;
+        }
+}
+
+// Column c (0..127) of the tile over rows rh*128 .. +127: 64 words, word i = rows (2i, 2i+1).
+__device__ __forceinline__ void load_col(uint32_t tile, int c, int rh, uint32_t (&w)[64])
+{
+    const uint32_t box = tile + (rh * 2 + (c >> 6)) * kBox;
+    const int j = (c & 63) >> 3, e = (c & 7) << 1;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const uint32_t lo = lds_u16(box + sw128(2 * i, j) + e);
+        const uint32_t hi = lds_u16(box + sw128(2 * i + 1, j) + e);
+        w[i] = lo | (hi << 16);
+    }
+}
+
+// 128 values (64 words) -> 8 code chunks written to row `r` of a swizzled staging box.
+__device__ __forceinline__ void write_codes(uint32_t box, int r, const uint32_t (&w)[64], const GroupScale &g)
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        sts_v4(box + sw128(r, q), codes16(&w[q * 8], g));
+}
+
 // ------------------------------------------------------------------ 1x128 rows
 //
-// Tile = 64 rows x 128 columns (16 KB).  Consumer warp w owns rows 8w .. 8w+7 of the tile,
-// a half-warp per row (16 lanes x 8 values); it copies its rows into registers, releases
-// the stage, then writes 8 codes per lane (128 contiguous bytes per half-warp) and the
-// 8 row scales with one store.
-constexpr int QR_ROWS = 64, QR_STAGES = 4, QR_TILE = QR_ROWS * 256;
-constexpr size_t QR_SMEM = ring_bytes<QR_STAGES, QR_TILE>();
+// Thread t of the consumers owns row t of the tile; warpgroup h (threads 128h .. +127)
+// owns rows 128h .. +127 and their staging box.
+constexpr int QR_STAGES = 2;
 
 template <bool POW2>
-__global__ void __launch_bounds__(kQThreads, 3)
-    quant_rows_kernel(const __grid_constant__ CUtensorMap tmx, const QuantArgs p)
+__global__ void __launch_bounds__(kQThreads, 1)
+    quant_rows_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
+                      const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QuantSmem sm = carve<QR_STAGES, QR_TILE>(smem_raw);
-    init_ring<QR_STAGES>(sm);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ncb = p.cols / 128, items = ((p.rows + QR_ROWS - 1) / QR_ROWS) * ncb;
+    const QSmem sm = q_carve<QR_STAGES, false>(smem_raw);
+    q_init<QR_STAGES>(sm);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
+    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
     const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
     if (warp == kConsumers) {
         if (lane == 0)
-            produce<QR_STAGES, QR_ROWS>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+            q_produce<QR_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
         return;
     }
-    const int half = lane >> 4, hl = lane & 15;
-    uint32_t it = 0;
+    const int h = t >> 7, rr = t & 127;
+    const uint32_t wgbar = sm.bars + 8 * (2 * QR_STAGES + h);
+    const uint32_t out = sm.out_rows + h * kBox;
+    const bool elected = rr == 0;
+    uint32_t cph = 0, it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const uint32_t st = it % QR_STAGES, ph = (it / QR_STAGES) & 1;
-        if (!mbar_wait(smem_u32(sm.bars + st), ph, ctl, 0x1200 | st))
+        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1200 | st))
             break;
         const int64_t rb = item / ncb, kb = item - rb * ncb;
-        const uint32_t tile = smem_u32(sm.stage + st * QR_TILE);
-        uint4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            v[i] = lds_v4(tile + (warp * 8 + 2 * i + half) * 256 + hl * 16);
+        uint32_t w[64];
+        load_row(sm.stage + st * kTile, t, w);
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(sm.bars + QR_STAGES + st));
-        uint2 cw[4];
-        const GroupScale mine = row_codes<4, POW2>(v, cw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t r = rb * QR_ROWS + warp * 8 + 2 * i + half;
-            if (r < p.rows)
-                *reinterpret_cast<uint2 *>(p.q + r * p.ldq + kb * 128 + hl * 8) = cw[i];
+            mbar_arrive(sm.bars + 8 * (QR_STAGES + st));
+        const GroupScale g = make_group_scale(amax_words(w), POW2);
+        const int64_t r = rb * kTileRows + t;
+        if (r < p.rows)
+            p.s[kb * p.lds + r] = g.s;
+        if (elected)
+            bulk_wait_read0();                 // the previous store has left the staging box
+        if (!wg_sync(wgbar, cph, ctl, 0x1210))
+            break;
+        write_codes(out, rr, w, g);
+        fence_proxy_async_smem();
+        if (!wg_sync(wgbar, cph, ctl, 0x1211))
+            break;
+        const int64_t y = rb * kTileRows + h * 128;
+        if (elected && y < p.rows) {
+            tma_store_2d(&tmq, out, static_cast<int32_t>(kb * 128), static_cast<int32_t>(y));
+            bulk_commit();
         }
-        const float my_s = mine.s;
-        const int64_t r = rb * QR_ROWS + warp * 8 + lane;
-        if (lane < 8 && r < p.rows)
-            p.s[kb * p.lds + r] = my_s;
     }
+    if (elected)
+        bulk_wait0();
 }
 
 // --------------------------------------------------- fused 1x128 + 128x1 (dual)
 //
-// Tile = 128 x 128 (32 KB).  Row groups: warp w owns rows 16w .. 16w+15 (half-warp per
-// row).  Column groups: thread t owns column t % 128 over rows 64 (t / 128) .. +63; the
-// two halves combine their max through shared memory.  After both passes have read the
-// tile into registers the stage is released; the column codes are transposed through a
-// padded shared tile and written as 128 contiguous bytes per output row.
-constexpr int QD_STAGES = 2, QD_TILE = 128 * 256;
-constexpr size_t QD_SMEM = ring_bytes<QD_STAGES, QD_TILE>() + 128 * kQtPitch + 2 * 128 * 4;
+// Row groups as in the row kernel; then thread t owns column t % 128 over the 128 rows of
+// warpgroup half t / 128 (one 128x1 group) and writes its codes as row (t % 128) of the
+// transposed staging box of that half.
+constexpr int QD_STAGES = 2;
 
 template <bool POW2, bool ROWS>
-__global__ void __launch_bounds__(kQThreads, 2)
-    quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, const QuantArgs p)
+__global__ void __launch_bounds__(kQThreads, 1)
+    quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
+                      const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QuantSmem sm = carve<QD_STAGES, QD_TILE>(smem_raw);
-    uint8_t *qts = sm.extra;
-    float *colmax = reinterpret_cast<float *>(sm.extra + 128 * kQtPitch);
-    init_ring<QD_STAGES>(sm);
+    const QSmem sm = q_carve<QD_STAGES, true>(smem_raw);
+    q_init<QD_STAGES>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
-    const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;
+    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
     const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
     if (warp == kConsumers) {
         if (lane == 0)
-            produce<QD_STAGES, 128>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+            q_produce<QD_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
         return;
     }
-    const int half = lane >> 4, hl = lane & 15;
-    const int c = t & 127, h = t >> 7;
-    const uint32_t cbar = smem_u32(sm.bars + 2 * QD_STAGES);
-    uint32_t cph = 0;  // consumer-barrier phase counter
-    uint32_t it = 0;
+    const int h = t >> 7, rr = t & 127;
+    const uint32_t wgbar = sm.bars + 8 * (2 * QD_STAGES + h);
+    const uint32_t out_r = sm.out_rows + h * kBox, out_c = sm.out_cols + h * kBox;
+    const bool elected = rr == 0;
+    uint32_t cph = 0, it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const uint32_t st = it % QD_STAGES, ph = (it / QD_STAGES) & 1;
-        if (!mbar_wait(smem_u32(sm.bars + st), ph, ctl, 0x1300 | st))
+        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1300 | st))
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
-        const int64_t r0 = rb * 128, c0 = cb * 128;
-        const uint32_t tile = smem_u32(sm.stage + st * QD_TILE);
-
+        const uint32_t tile = sm.stage + st * kTile;
+        const int64_t y = rb * kTileRows + h * 128;       // first row of this warpgroup's half
+        const bool half_in = y < p.rows;                   // rows is a multiple of 128
+        if (elected)
+            bulk_wait_read0();                             // both staging boxes are free
+        if (!wg_sync(wgbar, cph, ctl, 0x1310))
+            break;
+        uint32_t w[64];
         if (ROWS) {
-            // row groups first, so their registers are free before the column pass
-            uint4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = lds_v4(tile + (warp * 16 + 2 * i + half) * 256 + hl * 16);
-            uint2 cw[8];
-            const GroupScale mine = row_codes<8, POW2>(v, cw);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = warp * 16 + 2 * i + half;
-                *reinterpret_cast<uint2 *>(p.q + (r0 + r) * p.ldq + c0 + hl * 8) = cw[i];
-            }
-            const float my_s = mine.s;
-            if (lane < 16)
-                p.s[cb * p.lds + r0 + warp * 16 + lane] = my_s;
+            load_row(tile, t, w);
+            const GroupScale g = make_group_scale(amax_words(w), POW2);
+            if (half_in)
+                p.s[cb * p.lds + y + rr] = g.s;
+            write_codes(out_r, rr, w, g);
         }
-        float col[64];
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            col[i] = __uint_as_float(lds_u16(tile + (h * 64 + i) * 256 + c * 2) << 16);
-            a = fmaxf(a, fabsf(col[i]));
-        }
-        colmax[h * 128 + c] = a;
-        if (!consumers_sync(cbar, cph, ctl, 0x1310))  // tile fully read, column halves published
-            break;
+        load_col(tile, rr, h, w);
+        __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(sm.bars + QD_STAGES + st));
-
-        a = fmaxf(colmax[c], colmax[128 + c]);
-        const GroupScale g = make_group_scale(a, POW2);
-        if (h == 0)
-            p.sT[rb * p.ldsT + c0 + c] = g.s;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = j * 16 + 4 * k;
-                w[k] = e4m3_pair(col[i], col[i + 1], g) | (e4m3_pair(col[i + 2], col[i + 3], g) << 16);
-            }
-            *reinterpret_cast<uint4 *>(qts + c * kQtPitch + h * 64 + j * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            mbar_arrive(sm.bars + 8 * (QD_STAGES + st));   // this warp has read the tile
+        {
+            const GroupScale g = make_group_scale(amax_words(w), POW2);
+            if (half_in)
+                p.sT[(y / 128) * p.ldsT + cb * 128 + rr] = g.s;
+            write_codes(out_c, rr, w, g);
         }
-        if (!consumers_sync(cbar, cph, ctl, 0x1311))  // transposed tile complete
+        fence_proxy_async_smem();
+        if (!wg_sync(wgbar, cph, ctl, 0x1311))
             break;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int id = t + k * 256;
-            const int rr = id >> 3, part = id & 7;
-            *reinterpret_cast<uint4 *>(p.qT + (c0 + rr) * p.ldqT + r0 + part * 16) =
-                *reinterpret_cast<const uint4 *>(qts + rr * kQtPitch + part * 16);
+        if (elected && half_in) {
+            if (ROWS)
+                tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
+            tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
+            bulk_commit();
         }
-        if (!consumers_sync(cbar, cph, ctl, 0x1312))  // transposed tile and colmax free again
-            break;
     }
+    if (elected)
+        bulk_wait0();
 }
 
 // ------------------------------------------------------------------ 128x128 blocks
 //
-// Tile = one block (32 KB).  Each consumer thread copies its 64 values into registers;
-// the block max goes through warp shuffles and one shared reduction; the stage is
-// released before the codes are computed.  Optional transposed codes are gathered through
-// two padded shared tiles.
-constexpr int QB_STAGES = 2, QB_TILE = 128 * 256;
-constexpr size_t QB_SMEM = ring_bytes<QB_STAGES, QB_TILE>() + 2 * 128 * kQtPitch + 64;
+// The 256-row tile holds two blocks; warpgroup h owns block h: each thread its row, the
+// block max through warp shuffles and a 4-warp shared reduction.  Transposed codes are
+// gathered column-wise from the row-code staging box.
+constexpr int QB_STAGES = 2;
 
 template <bool POW2, bool TRANS>
-__global__ void __launch_bounds__(kQThreads, 2)
-    quant_block_kernel(const __grid_constant__ CUtensorMap tmx, const QuantArgs p)
+__global__ void __launch_bounds__(kQThreads, 1)
+    quant_block_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
+                       const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QuantSmem sm = carve<QB_STAGES, QB_TILE>(smem_raw);
-    uint8_t *cs = sm.extra;
-    uint8_t *qts = sm.extra + 128 * kQtPitch;
-    float *red = reinterpret_cast<float *>(sm.extra + 2 * 128 * kQtPitch);
-    init_ring<QB_STAGES>(sm);
+    const QSmem sm = q_carve<QB_STAGES, TRANS>(smem_raw);
+    q_init<QB_STAGES>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
-    const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;
+    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
     const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
     if (warp == kConsumers) {
         if (lane == 0)
-            produce<QB_STAGES, 128>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+            q_produce<QB_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
         return;
     }
-    const int half = lane >> 4, hl = lane & 15;
-    const uint32_t cbar = smem_u32(sm.bars + 2 * QB_STAGES);
-    uint32_t cph = 0;  // consumer-barrier phase counter
-    uint32_t it = 0;
+    const int h = t >> 7, rr = t & 127;
+    const uint32_t wgbar = sm.bars + 8 * (2 * QB_STAGES + h);
+    const uint32_t out_r = sm.out_rows + h * kBox, out_c = sm.out_cols + h * kBox;
+    const bool elected = rr == 0;
+    uint32_t cph = 0, it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const uint32_t st = it % QB_STAGES, ph = (it / QB_STAGES) & 1;
-        if (!mbar_wait(smem_u32(sm.bars + st), ph, ctl, 0x1400 | st))
+        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1400 | st))
             break;
-        const int64_t bi = item / ncb, bj = item - bi * ncb;
-        const int64_t r0 = bi * 128, c0 = bj * 128;
-        const uint32_t tile = smem_u32(sm.stage + st * QB_TILE);
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = lds_v4(tile + (warp * 16 + 2 * i + half) * 256 + hl * 16);
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            a = fmaxf(a, amax8(v[i]));
+        const int64_t rb = item / ncb, cb = item - rb * ncb;
+        const int64_t y = rb * kTileRows + h * 128;        // first row of this block
+        const bool block_in = y < p.rows;                   // rows is a multiple of 128
+        uint32_t w[64];
+        load_row(sm.stage + st * kTile, t, w);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(sm.bars + 8 * (QB_STAGES + st));
+        float a = amax_words(w);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         if (lane == 0)
-            red[warp] = a;
-        if (!consumers_sync(cbar, cph, ctl, 0x1410))  // block max published, tile read
+            sm.red[warp] = a;
+        if (elected)
+            bulk_wait_read0();                              // the staging boxes are free
+        if (!wg_sync(wgbar, cph, ctl, 0x1410))             // block max published
             break;
-        if (lane == 0)
-            mbar_arrive(smem_u32(sm.bars + QB_STAGES + st));
-        a = red[0];
-#pragma unroll
-        for (int k = 1; k < kConsumers; ++k)
-            a = fmaxf(a, red[k]);
+        a = fmaxf(fmaxf(sm.red[h * 4], sm.red[h * 4 + 1]), fmaxf(sm.red[h * 4 + 2], sm.red[h * 4 + 3]));
         const GroupScale g = make_group_scale(a, POW2);
-        if (t == 0)
-            p.s[bi * p.lds + bj] = g.s;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = warp * 16 + 2 * i + half;
-            const uint2 cw = codes8(v[i], g);
-            *reinterpret_cast<uint2 *>(p.q + (r0 + r) * p.ldq + c0 + hl * 8) = cw;
-            if (TRANS)
-                *reinterpret_cast<uint2 *>(cs + r * kQtPitch + hl * 8) = cw;
-        }
+        if (rr == 0 && block_in)
+            p.s[(y / 128) * p.lds + cb] = g.s;
+        write_codes(out_r, rr, w, g);
         if (TRANS) {
-            if (!consumers_sync(cbar, cph, ctl, 0x1411))  // row-major codes complete
+            if (!wg_sync(wgbar, cph, ctl, 0x1411))         // row codes complete
                 break;
-            const int c = t & 127, h = t >> 7;
+            // column rr of the block: bytes (row i, col rr) of the staging box
+            const int j = rr >> 4, e = rr & 15;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int q = 0; q < 8; ++q) {
                 uint32_t wd[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int i = h * 64 + j * 16 + k * 4;
-                    wd[k] = static_cast<uint32_t>(cs[i * kQtPitch + c]) |
-                            (static_cast<uint32_t>(cs[(i + 1) * kQtPitch + c]) << 8) |
-                            (static_cast<uint32_t>(cs[(i + 2) * kQtPitch + c]) << 16) |
-                            (static_cast<uint32_t>(cs[(i + 3) * kQtPitch + c]) << 24);
+                    const int i = q * 16 + k * 4;
+                    wd[k] = lds_u8(out_r + sw128(i, j) + e) | (lds_u8(out_r + sw128(i + 1, j) + e) << 8) |
+                            (lds_u8(out_r + sw128(i + 2, j) + e) << 16) | (lds_u8(out_r + sw128(i + 3, j) + e) << 24);
                 }
-                *reinterpret_cast<uint4 *>(qts + c * kQtPitch + h * 64 + j * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            }
-            if (!consumers_sync(cbar, cph, ctl, 0x1412))  // transposed tile complete
-                break;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int id = t + k * 256;
-                const int rr = id >> 3, part = id & 7;
-                *reinterpret_cast<uint4 *>(p.qT + (c0 + rr) * p.ldqT + r0 + part * 16) =
-                    *reinterpret_cast<const uint4 *>(qts + rr * kQtPitch + part * 16);
+                sts_v4(out_c + sw128(rr, q), make_uint4(wd[0], wd[1], wd[2], wd[3]));
             }
         }
-        if (!consumers_sync(cbar, cph, ctl, 0x1413))  // shared tiles and red[] free again
+        fence_proxy_async_smem();
+        if (!wg_sync(wgbar, cph, ctl, 0x1412))
             break;
+        if (elected && block_in) {
+            tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
+            if (TRANS)
+                tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
+            bulk_commit();
+        }
     }
+    if (elected)
+        bulk_wait0();
 }
 
-template <class K>
-cudaError_t launch_q(K kern, size_t smem, int per_sm, int64_t items, int num_sms, const CUtensorMap &tm,
-                     const QuantArgs &a, cudaStream_t st)
+template <class K, class... Args>
+cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream_t st, Args... args)
 {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
-    if (items < grid)
-        grid = items;
-    kern<<<static_cast<int>(grid), kQThreads, smem, st>>>(tm, a);
+    const int64_t grid = items < num_sms ? items : num_sms;
+    kern<<<static_cast<int>(grid), kQThreads, smem, st>>>(args...);
     return cudaGetLastError();
 }
 
 } // namespace
 
-cudaError_t launch_quant_rows(const CUtensorMap &tm, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
+cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
+                              int num_sms, cudaStream_t st)
 {
-    const int64_t items = ((a.rows + QR_ROWS - 1) / QR_ROWS) * (a.cols / 128);
+    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
     if (items == 0)
         return cudaSuccess;
-    return pow2 ? launch_q(quant_rows_kernel<true>, QR_SMEM, 3, items, num_sms, tm, a, st)
-                : launch_q(quant_rows_kernel<false>, QR_SMEM, 3, items, num_sms, tm, a, st);
+    constexpr size_t smem = q_smem_bytes<QR_STAGES, false>();
+    return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, tmx, tmq, a)
+                : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, tmx, tmq, a);
 }
 
-cudaError_t launch_quant_dual(const CUtensorMap &tm, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
+cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
+                              const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
 {
-    const int64_t items = (a.rows / 128) * (a.cols / 128);
+    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
     if (items == 0)
         return cudaSuccess;
+    constexpr size_t smem = q_smem_bytes<QD_STAGES, true>();
     const bool rows_out = a.q != nullptr;
     if (pow2)
-        return rows_out ? launch_q(quant_dual_kernel<true, true>, QD_SMEM, 2, items, num_sms, tm, a, st)
-                        : launch_q(quant_dual_kernel<true, false>, QD_SMEM, 2, items, num_sms, tm, a, st);
-    return rows_out ? launch_q(quant_dual_kernel<false, true>, QD_SMEM, 2, items, num_sms, tm, a, st)
-                    : launch_q(quant_dual_kernel<false, false>, QD_SMEM, 2, items, num_sms, tm, a, st);
+        return rows_out ? launch_q(quant_dual_kernel<true, true>, smem, items, num_sms, st, tmx, tmq, tmqT, a)
+                        : launch_q(quant_dual_kernel<true, false>, smem, items, num_sms, st, tmx, tmq, tmqT, a);
+    return rows_out ? launch_q(quant_dual_kernel<false, true>, smem, items, num_sms, st, tmx, tmq, tmqT, a)
+                    : launch_q(quant_dual_kernel<false, false>, smem, items, num_sms, st, tmx, tmq, tmqT, a);
 }
 
-cudaError_t launch_quant_block(const CUtensorMap &tm, const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
+cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
+                               const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
 {
-    const int64_t items = (a.rows / 128) * (a.cols / 128);
+    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
     if (items == 0)
         return cudaSuccess;
     const bool tr = a.qT != nullptr;
+    constexpr size_t smem_t = q_smem_bytes<QB_STAGES, true>();
+    constexpr size_t smem_n = q_smem_bytes<QB_STAGES, false>();
     if (pow2)
-        return tr ? launch_q(quant_block_kernel<true, true>, QB_SMEM, 2, items, num_sms, tm, a, st)
-                  : launch_q(quant_block_kernel<true, false>, QB_SMEM, 2, items, num_sms, tm, a, st);
-    return tr ? launch_q(quant_block_kernel<false, true>, QB_SMEM, 2, items, num_sms, tm, a, st)
-              : launch_q(quant_block_kernel<false, false>, QB_SMEM, 2, items, num_sms, tm, a, st);
+        return tr ? launch_q(quant_block_kernel<true, true>, smem_t, items, num_sms, st, tmx, tmq, tmqT, a)
+                  : launch_q(quant_block_kernel<true, false>, smem_n, items, num_sms, st, tmx, tmq, tmqT, a);
+    return tr ? launch_q(quant_block_kernel<false, true>, smem_t, items, num_sms, st, tmx, tmq, tmqT, a)
+              : launch_q(quant_block_kernel<false, false>, smem_n, items, num_sms, st, tmx, tmq, tmqT, a);
 }
 
 } // namespace mpq

@@ -50,6 +50,37 @@ def _adversarial(rows=200, cols=512, seed=0):
     return x.to(torch.bfloat16)
 
 
+def _sweep_rows():
+    """Every finite BF16 value x, each under many group scales: row = [amax, 127 values with
+    |x| <= amax].  The max-abs values span the binary32 range, with significands 1, 1.75
+    (the power-of-2 exponent step), just above 1.75 and all ones, and bracket 448 * 2^-80,
+    below which the kernels switch from the multiply-and-correct path to IEEE division."""
+    bits = np.arange(0x10000, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    vals = np.sort(vals[np.isfinite(vals)].astype(np.float32))
+    amaxes = []
+    for e in list(range(-133, 127, 9)) + [-72, -71, -70, -69, -8, 0, 8]:
+        for sig in (1.0, 1.75, 1.7578125, 1.9921875):
+            a = np.float32(np.ldexp(sig, e))
+            if np.isfinite(a) and a > 0:
+                amaxes.append(a)
+    rows = []
+    for a in amaxes:
+        v = vals[np.abs(vals) <= a]
+        v = np.concatenate([v, np.zeros((-len(v)) % 127, np.float32)]).reshape(-1, 127)
+        rows.append(np.concatenate([np.full((len(v), 1), a, np.float32), v], axis=1))
+    x = torch.from_numpy(np.concatenate(rows)).to(torch.bfloat16)
+    # the amax entries are BF16-exact; shuffle each row so the amax is not always in column 0
+    g = torch.Generator().manual_seed(11)
+    perm = torch.argsort(torch.rand(x.shape, generator=g), dim=1)
+    return torch.gather(x, 1, perm)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_tile_rows_every_bf16_value(mpq, pow2):
+    _rows_parity(mpq, _sweep_rows(), pow2)
+
+
 @pytest.mark.parametrize("pow2", [False, True])
 def test_tile_rows_tiny_config(mpq, pow2):
     _rows_parity(mpq, workloads.tiny_fprop()["A"], pow2)
