@@ -13,13 +13,15 @@
 //   transposed weight), per-row [K/128][N] (Wgrad, 128x1 token tiles).
 //
 // Design (B300, persistent, one CTA per SM, 128 x 256 output tile per CTA).  Two modes:
-//   pair   (default) a cluster of two CTAs on two SMs works on vertically adjacent tiles
-//          that share the same 256 rows of B: each CTA loads its own 128 rows of A and
-//          one half (128 rows) of B per 128-K slice and multicasts that half into both
-//          CTAs' shared memory, so each SM pulls 32 KB per slice from L2 instead of 48 KB.
-//          A stage is refilled only when both CTAs' MMAs released it (commit multicast to
-//          both); everything else (MMA, TMEM hand-off, promotion) stays on each SM.
-//   single one CTA loads all of its A and B slices itself.
+//   pair   (default) a cluster of two CTAs on two SMs computes one 256 x 256 tile with
+//          2-SM MMAs (cta_group::2, M = 256): each CTA stages its own 128 rows of A and
+//          one half (128 rows) of B per 128-K slice -- 32 KB per stage instead of 48 KB,
+//          so each SM's shared memory carries a third less operand traffic, the limit of
+//          the single-SM form -- and the even CTA issues the MMAs, which write the
+//          accumulators of both SMs.  Both CTAs' loads complete on the even CTA's stage
+//          barrier; its commits release the stage and hand over the partial in both CTAs;
+//          both CTAs' promotion warps release the partial buffer to it.
+//   single one CTA loads all of its A and B slices itself (M = 128 MMAs).
 // Roles in each CTA:
 //   warp 0      TMA producer: E4M3 slices into a shared-memory ring (128-byte swizzle);
 //   warp 1      MMA issuer: four MMAs (K = 32 each) per 128-K slice into one of two TMEM
@@ -49,9 +51,9 @@ constexpr int kMaxGroups = 1024;
 
 template <bool PAIR>
 struct Cfg {
-    static constexpr int STAGES = 4;
-    static constexpr int B_ROWS = PAIR ? 128 : 256;          // B rows loaded by one CTA per slice
-    static constexpr uint32_t B_BYTES = BN * BK;             // the full B slice in each CTA
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int B_ROWS = PAIR ? 128 : 256;          // B rows staged by one CTA per slice
+    static constexpr uint32_t B_BYTES = B_ROWS * BK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TILE_M = PAIR ? 256 : 128;          // rows per tile (both CTAs of a pair)
     static constexpr int BAR_FULL = 0;
@@ -142,11 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(C::BAR_FULL + s), 1);
-            mbar_init(bar(C::BAR_EMPTY + s), PAIR ? 2 : 1);   // both CTAs' MMAs release a stage
+            mbar_init(bar(C::BAR_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::BAR_TFULL + b), 1);
-            mbar_init(bar(C::BAR_TEMPTY + b), 8);
+            mbar_init(bar(C::BAR_TEMPTY + b), PAIR ? 16 : 8);   // promotion warps of the pair
         }
         for (int j = 0; j < SSLOTS; ++j) {
             mbar_init(bar(C::BAR_SFULL + j), 32);
@@ -162,8 +164,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(misc), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(misc), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(misc), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (GROUPED && warp == 2) {
         // Expert schedule: offsets clamped into [0, M] and made monotone (running max),
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (PAIR)
-        cluster_sync_all();  // the peer's barriers are initialised before any multicast lands
+        cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
 
@@ -268,21 +275,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, ctl, 0x0100 | s))
                         goto producer_done;
-                    mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::STAGE_BYTES);
-                    tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, bar(C::BAR_FULL + s), kb * BK, ti.row0);
-                    if (PAIR)
-                        tma_load_2d_mc(smem_u32(smB + s * C::B_BYTES + rank * (C::B_ROWS * BK)), &tmB,
-                                       bar(C::BAR_FULL + s), kb * BK, ti.brow0, 0x3);
-                    else
+                    if (PAIR) {
+                        // both CTAs' slices complete on the even CTA's stage barrier
+                        const uint32_t full = mapa_shared(bar(C::BAR_FULL + s), 0);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(bar(C::BAR_FULL + s), 2 * C::STAGE_BYTES);
+                        tma_load_2d_pair(smem_u32(smA + s * A_BYTES), &tmA, full, kb * BK, ti.row0);
+                        tma_load_2d_pair(smem_u32(smB + s * C::B_BYTES), &tmB, full, kb * BK, ti.brow0);
+                    } else {
+                        mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::STAGE_BYTES);
+                        tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, bar(C::BAR_FULL + s), kb * BK, ti.row0);
                         tma_load_2d(smem_u32(smB + s * C::B_BYTES), &tmB, bar(C::BAR_FULL + s), kb * BK, ti.brow0);
+                    }
                 }
             }
         producer_done:
-            for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-                mbar_wait_drain(bar(C::BAR_FULL + j % STAGES), (j / STAGES) & 1, p.timeout_ns);
-        } else if (warp == 1 && lane == 0) {
+            if (!PAIR || rank == 0) {
+                for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+                    mbar_wait_drain(bar(C::BAR_FULL + j % STAGES), (j / STAGES) & 1, p.timeout_ns);
+            } else if (*abort_flag) {
+                // The odd CTA's copies complete on the even CTA's barriers; after a timeout
+                // give copies still in flight a grace period before this CTA exits.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+        } else if (warp == 1 && lane == 0 && rank == 0) {
             // ---------------------------------------------------------- MMA issuer
-            const uint32_t idesc = idesc_e4m3_f32(128, BN);
+            const uint32_t idesc = idesc_e4m3_f32(PAIR ? 256 : 128, BN);
             uint32_t it = 0;
             for (int t = unit; t < T; t += nunits) {
                 for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -297,18 +317,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
                     const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        umma_e4m3(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
-                                  k > 0 ? 1u : 0u);
-                    if (PAIR)
-                        umma_commit_mc(bar(C::BAR_EMPTY + s), 0x3);   // release the stage in both CTAs
-                    else
+                    for (int k = 0; k < BK / 32; ++k) {
+                        if (PAIR)
+                            umma_e4m3_pair(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
+                                           k > 0 ? 1u : 0u);
+                        else
+                            umma_e4m3(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
+                                      k > 0 ? 1u : 0u);
+                    }
+                    if (PAIR) {
+                        umma_commit_pair_mc(bar(C::BAR_EMPTY + s), 0x3);   // the stage is free in both CTAs
+                        umma_commit_pair_mc(bar(C::BAR_TFULL + buf), 0x3); // the partial is ready in both
+                    } else {
                         umma_commit(bar(C::BAR_EMPTY + s));
-                    umma_commit(bar(C::BAR_TFULL + buf));
+                        umma_commit(bar(C::BAR_TFULL + buf));
+                    }
                 }
             }
         mma_done:
-            umma_commit(bar(C::BAR_DRAIN));
+            if (PAIR)
+                umma_commit_pair_mc(bar(C::BAR_DRAIN), 0x1);
+            else
+                umma_commit(bar(C::BAR_DRAIN));
             mbar_wait_drain(bar(C::BAR_DRAIN), 0, p.timeout_ns);
         } else if (warp == 2) {
             // ---------------------------------------------------------- scale loader
@@ -396,7 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(C::BAR_TEMPTY + buf));
+                    if (PAIR)
+                        mbar_arrive_remote(mapa_shared(bar(C::BAR_TEMPTY + buf), 0));   // the even CTA's
+                    else
+                        mbar_arrive(bar(C::BAR_TEMPTY + buf));
                     mbar_arrive(bar(C::BAR_SEMPTY + j));
                 }
             }
@@ -482,10 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (PAIR)
-        cluster_sync_all();  // no multicast into this CTA or commit from the peer is pending
+        cluster_sync_all();  // the pair's MMAs, copies and remote arrivals are all complete
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -258,10 +258,14 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly in a peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+// Arrive on an mbarrier given by its shared::cluster address (possibly in a peer CTA), with
+// release semantics at CTA scope only: it orders nothing in memory for the peer, so use it
+// where the protected resource is already drained (e.g. TMEM reads completed with
+// tcgen05.wait::ld).  A cluster-scope release would fence all of the thread's prior memory
+// traffic on every arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 2-D tiled load multicast to every CTA of `mask` in the cluster: the tile lands at the
@@ -291,6 +295,62 @@ __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask)
 
 // 2-D tiled store of a shared-memory box to global memory (clipped at the tensor bounds),
 // tracked by the executing thread's bulk async-group.
+// ---------------------------------------------------------------- CTA pairs (2-SM MMA)
+//
+// With cta_group::2 the even CTA of a cluster pair issues MMAs that read A and B from both
+// CTAs' shared memory (each holds M/2 rows of A and N/2 rows of B at the same offsets) and
+// write each CTA's TMEM (its M/2 rows, all N columns).  TMEM allocation is collective: one
+// warp of each CTA of the pair executes the same alloc / relinquish / dealloc.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A * B^T over both CTAs of the pair (issued by one thread of the even CTA).
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at the same offset in every CTA of `mask` when all prior
+// pair MMAs of this thread have completed.
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// TMA 2-D load into this CTA's shared memory whose completion is counted on an mbarrier
+// that may live in the peer CTA (`bar_cluster` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t bar_cluster, int32_t x,
+                                                 int32_t y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x, int32_t y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
