@@ -67,6 +67,8 @@ typedef enum mpq_dtype {
 
 /* Flags */
 #define MPQ_POW2 1u /* power-of-2 scales: s = 2^e, e the smallest integer with amax <= 448*2^e */
+#define MPQ_GROUPED_ROW_TILES 2u    /* grouped GEMM: tiles of token rows (many tokens per expert) */
+#define MPQ_GROUPED_WEIGHT_TILES 4u /* grouped GEMM: tiles of weight rows (few tokens per expert) */
 
 typedef struct mpq_handle_s *mpq_handle;
 
@@ -181,7 +183,17 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  *   B          [G][N][K] E4M3 (expert g at B + g*N*ldb), ldb >= K.
  *   sB         [G][N/128][ldsb] float32 (expert g at sB + g*(N/128)*ldsb), ldsb >= K/128.
  *   C          [M_total, N] BF16 or FP32, ldc >= N.
- *   flags      0 (reserved).
+ *   flags      0, MPQ_GROUPED_ROW_TILES or MPQ_GROUPED_WEIGHT_TILES: the tiling (below).
+ * Two tilings compute the same sums:
+ *   row tiles     tiles of 256 (or 128) token rows x 256 features, for experts with many
+ *                 tokens (prefill, training);
+ *   weight tiles  one 128-row block of an expert's weight against all of the expert's
+ *                 tokens (up to 256 per tile), the MMA sized to the token count: for the
+ *                 few tokens per expert of decoding, where streaming the weights from
+ *                 memory sets the pace.
+ * With flags 0 the library picks weight tiles when M_total <= 64 * G (at most 64 tokens
+ * per expert on average), else row tiles.  The two tilings may differ in the last bits
+ * of the FP32 accumulation (both are within the GEMM tolerance of the method).
  * Requirements: 1 <= G <= 1024; N % 128 == 0; K % 128 == 0; alignment as for
  * fp8_gemm_blockscaled.
  */

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libmpq.so")
 FPROP, DGRAD, WGRAD = 0, 1, 2
 OUT_BF16, OUT_FP32 = 0, 1
 POW2 = 1
+GROUPED_ROW_TILES, GROUPED_WEIGHT_TILES = 2, 4
 
 _STATUS = {0: "ok", 1: "null pointer argument", 2: "invalid size or leading dimension",
            3: "misaligned pointer or stride", 4: "unsupported op, dtype or flags",
@@ -195,11 +196,17 @@ def fp8_gemm_blockscaled(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Te
 
 def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,
                                  sB: torch.Tensor, *, out_dtype: int = OUT_BF16, C: Optional[torch.Tensor] = None,
-                                 stream=None):
+                                 tiles: str = "auto", stream=None):
     """MoE grouped FP8 GEMM: rows ``[off[g], off[g+1])`` of ``A`` use expert ``g``'s weight.
 
     ``offsets`` int64 CUDA ``[G+1]``; ``A [M, K]`` codes, ``sA [K/128, M]``; ``B [G, N, K]`` codes;
-    ``sB [G, N/128, K/128]``.  Rows outside every expert are left untouched in ``C``."""
+    ``sB [G, N/128, K/128]``.  Rows outside every expert are left untouched in ``C``.
+    ``tiles``: ``"rows"`` (token-row tiles, many tokens per expert), ``"weights"`` (weight-row
+    tiles sized to each expert's tokens, for decoding) or ``"auto"`` (weights when there are
+    at most 64 tokens per expert on average)."""
+    flags = {"auto": 0, "rows": GROUPED_ROW_TILES, "weights": GROUPED_WEIGHT_TILES}.get(tiles)
+    if flags is None:
+        raise ValueError("tiles: expected 'auto', 'rows' or 'weights'")
     _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
     if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.dim() == 1 and offsets.is_contiguous()):
         raise TypeError("offsets: expected a contiguous 1-D int64 CUDA tensor")
@@ -215,7 +222,7 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: tor
     C = _out(M, N, out_dtype, C, dev)
     st = _lib.fp8_grouped_gemm_blockscaled(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(A), _ld(A), _ptr(sA),
                                            _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
-                                           int(out_dtype), 0, _stream(dev, stream))
+                                           int(out_dtype), flags, _stream(dev, stream))
     _check("fp8_grouped_gemm_blockscaled", st)
     return C
 

@@ -351,7 +351,8 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
 {
     if (h == nullptr || d_offsets == nullptr)
         return MPQ_ERR_NULL;
-    if (flags != 0)
+    if ((flags & ~(MPQ_GROUPED_ROW_TILES | MPQ_GROUPED_WEIGHT_TILES)) != 0 ||
+        flags == (MPQ_GROUPED_ROW_TILES | MPQ_GROUPED_WEIGHT_TILES))
         return MPQ_ERR_UNSUPPORTED;
     mpq_status st = check_gemm_common(N, K, A, lda, sA, B, ldb, sB, C, ldc, out_dtype);
     if (st != MPQ_OK)
@@ -363,14 +364,8 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
         return MPQ_ERR_ALIGN;
     if (M_total == 0)
         return MPQ_OK;
-    CUtensorMap tmA, tmB;
-    if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
-        return st;
-    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
-        return st;
-    CUtensorMap tmC;
-    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
-        return st;
+    const bool weight_tiles =
+        (flags & MPQ_GROUPED_WEIGHT_TILES) != 0 || ((flags & MPQ_GROUPED_ROW_TILES) == 0 && M_total <= 64 * G);
     mpq::GemmArgs a{};
     a.M = M_total; a.N = N; a.K = K;
     a.sA = sA; a.ldsa = ldsa;
@@ -378,6 +373,22 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     a.C = C; a.ldc = ldc;
     a.offsets = d_offsets; a.G = static_cast<int>(G);
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tmA, tmB;
+    if (weight_tiles) {
+        if ((st = encode_operand(&tmA, A, M_total, K, lda, mpq::decode_x_box_rows())) != MPQ_OK)
+            return st;
+        if ((st = encode_operand(&tmB, B, G * N, K, ldb, 128)) != MPQ_OK)
+            return st;
+        return from_cuda(mpq::launch_decode(tmA, tmB, a, out_dtype == MPQ_OUT_FP32, h->num_sms,
+                                            static_cast<cudaStream_t>(stream)));
+    }
+    if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
+        return st;
+    CUtensorMap tmC;
+    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
+        return st;
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, h->gemm_pair,
                                       h->num_sms,
                                       static_cast<cudaStream_t>(stream)));

@@ -59,9 +59,11 @@ struct Cfg {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TILE_M = PAIR ? 256 : 128;          // rows per tile (both CTAs of a pair)
     static constexpr int BAR_FULL = 0;
-    static constexpr int BAR_EMPTY = BAR_FULL + STAGES;
-    static constexpr int BAR_TFULL = BAR_EMPTY + STAGES;
-    static constexpr int BAR_TEMPTY = BAR_TFULL + 2;
+    // DONE[s]: the MMAs of the slice held in stage s have completed -- the stage may be
+    // refilled and the slice's partial may be promoted.  One commit per slice serves both
+    // (every tcgen05.commit costs the tensor pipe a bubble).
+    static constexpr int BAR_DONE = BAR_FULL + STAGES;
+    static constexpr int BAR_TEMPTY = BAR_DONE + STAGES;
     static constexpr int BAR_SFULL = BAR_TEMPTY + 2;
     static constexpr int BAR_SEMPTY = BAR_SFULL + SSLOTS;
     static constexpr int BAR_DRAIN = BAR_SEMPTY + SSLOTS;
@@ -147,10 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(C::BAR_FULL + s), 1);
-            mbar_init(bar(C::BAR_EMPTY + s), 1);
+            mbar_init(bar(C::BAR_DONE + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(C::BAR_TFULL + b), 1);
             mbar_init(bar(C::BAR_TEMPTY + b), PAIR ? 16 : 8);   // promotion warps of the pair
         }
         for (int j = 0; j < SSLOTS; ++j) {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile ti = tile_of(t);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, ctl, 0x0100 | s))
+                    if (!mbar_wait(bar(C::BAR_DONE + s), ph ^ 1, ctl, 0x0100 | s))
                         goto producer_done;
                     if (PAIR) {
                         // both CTAs' slices complete on the even CTA's stage barrier
@@ -328,13 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_e4m3(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
                                       k > 0 ? 1u : 0u);
                     }
-                    if (PAIR) {
-                        umma_commit_pair_mc(bar(C::BAR_EMPTY + s), 0x3);   // the stage is free in both CTAs
-                        umma_commit_pair_mc(bar(C::BAR_TFULL + buf), 0x3); // the partial is ready in both
-                    } else {
-                        umma_commit(bar(C::BAR_EMPTY + s));
-                        umma_commit(bar(C::BAR_TFULL + buf));
-                    }
+                    if (PAIR)
+                        umma_commit_pair_mc(bar(C::BAR_DONE + s), 0x3);   // in both CTAs
+                    else
+                        umma_commit(bar(C::BAR_DONE + s));
                 }
             }
         mma_done:
@@ -397,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[i] = 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const uint32_t j = it % SSLOTS, sph = (it / SSLOTS) & 1;
-                const uint32_t buf = it & 1, tph = (it >> 1) & 1;
+                const uint32_t buf = it & 1;
+                const uint32_t ds = it % STAGES, dph = (it / STAGES) & 1;
                 if (!mbar_wait(bar(C::BAR_SFULL + j), sph, ctl, 0x0400 | j) ||
-                    !mbar_wait(bar(C::BAR_TFULL + buf), tph, ctl, 0x0410 | buf)) {
+                    !mbar_wait(bar(C::BAR_DONE + ds), dph, ctl, 0x0410 | ds)) {
                     ok = false;
                     break;
                 }

@@ -60,6 +60,14 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
 int gemm_b_box_rows(bool pair);
 
 // Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
+// Grouped GEMM for few tokens per expert (weights as the MMA's M operand, tokens as N):
+// tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
+// weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
+// the grouped launch_gemm (sB block scales [G][N/128][ldsb]); C is written directly.
+int decode_x_box_rows();
+cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &a, bool out_fp32,
+                          int num_sms, cudaStream_t st);
+
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);
 
 } // namespace mpq

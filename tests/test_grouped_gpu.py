@@ -18,11 +18,12 @@ def mpq():
     return m
 
 
-@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+@pytest.fixture(params=["rows_sm_pair", "rows_single_sm", "weights"])
 def tiles(request, mpq):
-    """Run the test with 256x256 tiles on SM pairs and with 128x256 tiles on single SMs."""
-    mpq.mpq_set_gemm_cta_pair(request.param)
-    yield request.param
+    """Run the test with token-row tiles (256x256 on SM pairs, 128x256 on single SMs) and
+    with weight-row tiles sized to each expert's tokens; yields the `tiles` argument."""
+    mpq.mpq_set_gemm_cta_pair(request.param != "rows_single_sm")
+    yield "weights" if request.param == "weights" else "rows"
     mpq.mpq_set_gemm_cta_pair(True)
 
 
@@ -56,7 +57,7 @@ def test_grouped_small(mpq, tiles, counts, lead, trail):
     qb, sb = _experts(G, N, K, 7 + G)
     C = torch.full((M, N), 12345.0, dtype=torch.float32, device="cuda")
     mpq.fp8_grouped_gemm_blockscaled(_dev(off.astype(np.int64)), _dev(qa), _dev(sa), _dev(qb), _dev(sb),
-                                     out_dtype=mpq.OUT_FP32, C=C)
+                                     out_dtype=mpq.OUT_FP32, C=C, tiles=tiles)
     ref, absref = oracle.grouped_gemm_ref(off, qa, sa, qb, sb)
     got = C.cpu().numpy().astype(np.float64)
     rows = np.zeros(M, bool)
@@ -66,7 +67,8 @@ def test_grouped_small(mpq, tiles, counts, lead, trail):
 
 
 def test_grouped_equals_single_gemms(mpq, tiles):
-    """Cross-path invariant: each expert's rows equal a single-GEMM call, bit for bit."""
+    """Cross-path invariant: with token-row tiles each expert's rows equal a single-GEMM
+    call bit for bit; with weight-row tiles they agree within the GEMM tolerance."""
     counts = [70, 300, 0, 129]
     G, N, K = len(counts), 384, 256
     off = np.concatenate([[0], np.cumsum(counts)])
@@ -75,17 +77,23 @@ def test_grouped_equals_single_gemms(mpq, tiles):
     a = (torch.randn((M, K), generator=g) * 3).to(torch.bfloat16)
     qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
     qb, sb = _experts(G, N, K, 5)
-    C = mpq.fp8_grouped_gemm_blockscaled(_dev(off.astype(np.int64)), _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    C = mpq.fp8_grouped_gemm_blockscaled(_dev(off.astype(np.int64)), _dev(qa), _dev(sa), _dev(qb), _dev(sb),
+                                         out_dtype=mpq.OUT_FP32, tiles=tiles)
     for e in range(G):
         if counts[e] == 0:
             continue
         r = slice(int(off[e]), int(off[e + 1]))
         Ce = mpq.fp8_gemm_blockscaled(mpq.FPROP, _dev(qa[r]), _dev(np.ascontiguousarray(sa[:, r])), _dev(qb[e]),
-                                      _dev(sb[e]))
-        assert torch.equal(C[r], Ce), f"expert {e}"
+                                      _dev(sb[e]), out_dtype=mpq.OUT_FP32)
+        if tiles == "rows":
+            assert torch.equal(C[r], Ce), f"expert {e}"
+        else:
+            ref, absref = oracle.gemm_ref(oracle.FPROP, qa[r], np.ascontiguousarray(sa[:, r]), qb[e], sb[e])
+            assert_gemm_close(C[r].cpu().numpy().astype(np.float64), ref, absref, f"expert {e}")
+            assert_gemm_close(Ce.cpu().numpy().astype(np.float64), ref, absref, f"single {e}")
 
 
-def _sampled_moe_check(mpq, d, proj, pow2_input):
+def _sampled_moe_check(mpq, d, proj, pow2_input, tiles="auto"):
     """Run one projection on the GPU end to end (quantize rows 1x128 + grouped GEMM) and
     check sampled rows of three experts (largest, median, smallest non-empty) against the
     oracle run from the same BF16 inputs."""
@@ -98,7 +106,7 @@ def _sampled_moe_check(mpq, d, proj, pow2_input):
     sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
     for e in range(G):
         mpq.fp8_quant_block_128x128(Wt[e], q=qw[e], s=sw[e])
-    C = mpq.fp8_grouped_gemm_blockscaled(off.cuda(), qx, sx, qw, sw)
+    C = mpq.fp8_grouped_gemm_blockscaled(off.cuda(), qx, sx, qw, sw, tiles=tiles)
     torch.cuda.synchronize()
     counts = d["counts"].numpy()
     nz = np.nonzero(counts)[0]
@@ -121,7 +129,8 @@ def test_moe_prefill_full_size_sampled(mpq):
     _sampled_moe_check(mpq, d, "down", True)
 
 
-def test_moe_decode_full_size_sampled(mpq):
+@pytest.mark.parametrize("tiles", ["weights", "rows"])
+def test_moe_decode_full_size_sampled(mpq, tiles):
     d = workloads.moe_decode(device="cuda")
-    _sampled_moe_check(mpq, d, "up", False)
-    _sampled_moe_check(mpq, d, "down", True)
+    _sampled_moe_check(mpq, d, "up", False, tiles)
+    _sampled_moe_check(mpq, d, "down", True, tiles)
