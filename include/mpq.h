@@ -37,6 +37,7 @@
 #ifndef MPQ_H
 #define MPQ_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -50,7 +51,8 @@ typedef enum mpq_status {
     MPQ_ERR_ALIGN = 3,       /* a pointer or stride breaks the 16-byte (or 4-byte) rule    */
     MPQ_ERR_UNSUPPORTED = 4, /* unknown op, dtype or flag combination                     */
     MPQ_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed                       */
-    MPQ_ERR_TIMEOUT = 6      /* a device-side wait ran out (reported by the status word)  */
+    MPQ_ERR_TIMEOUT = 6,     /* a device-side wait ran out (reported by the status word)  */
+    MPQ_ERR_WORKSPACE = 7    /* no workspace set on the handle, or it is too small        */
 } mpq_status;
 
 typedef enum mpq_op {
@@ -69,6 +71,7 @@ typedef enum mpq_dtype {
 #define MPQ_POW2 1u /* power-of-2 scales: s = 2^e, e the smallest integer with amax <= 448*2^e */
 #define MPQ_GROUPED_ROW_TILES 2u    /* grouped GEMM: tiles of token rows (many tokens per expert) */
 #define MPQ_GROUPED_WEIGHT_TILES 4u /* grouped GEMM: tiles of weight rows (few tokens per expert) */
+#define MPQ_FUSE_QUANT_A 8u         /* grouped GEMM: A is BF16, quantized 1x128 inside the launch */
 
 typedef struct mpq_handle_s *mpq_handle;
 
@@ -94,6 +97,23 @@ mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
  * B (weight) rows; each CTA loads half of the B slice and multicasts it to both.  0: every
  * CTA loads its own operands.  The results are bit-identical. */
 mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
+
+/*
+ * mpq_set_workspace -- hands the handle a caller-owned device buffer for calls that need
+ * scratch memory (today: fp8_grouped_gemm_blockscaled with MPQ_FUSE_QUANT_A, which keeps
+ * the quantized activations there).  The library never allocates it, frees it or keeps
+ * it past mpq_destroy; ptr must be 256-byte aligned and stay valid while calls that use it
+ * are in flight.  Calls on one handle that use the workspace must not overlap (on
+ * different streams) -- they share it.  ptr = NULL, bytes = 0 removes it.
+ */
+mpq_status mpq_set_workspace(mpq_handle h, void *ptr, size_t bytes);
+
+/*
+ * mpq_grouped_fused_workspace_bytes -- workspace bytes fp8_grouped_gemm_blockscaled needs
+ * with MPQ_FUSE_QUANT_A for M_total token rows, reduction length K and G experts:
+ * M_total*K codes + (K/128)*M_total scales + G counters, each part 256-byte aligned.
+ */
+mpq_status mpq_grouped_fused_workspace_bytes(int64_t M_total, int64_t K, int64_t G, size_t *bytes);
 
 /* Synchronize `stream`, read and clear the device status word.  Returns MPQ_OK or the
  * recorded error (MPQ_ERR_TIMEOUT); *where_out (may be NULL) receives the tag of the
@@ -183,7 +203,9 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  *   B          [G][N][K] E4M3 (expert g at B + g*N*ldb), ldb >= K.
  *   sB         [G][N/128][ldsb] float32 (expert g at sB + g*(N/128)*ldsb), ldsb >= K/128.
  *   C          [M_total, N] BF16 or FP32, ldc >= N.
- *   flags      0, MPQ_GROUPED_ROW_TILES or MPQ_GROUPED_WEIGHT_TILES: the tiling (below).
+ *   flags      0, MPQ_GROUPED_ROW_TILES or MPQ_GROUPED_WEIGHT_TILES: the tiling (below);
+ *              MPQ_FUSE_QUANT_A (optionally with MPQ_POW2): fused activation quantization
+ *              (below).
  * Two tilings compute the same sums:
  *   row tiles     tiles of 256 (or 128) token rows x 256 features, for experts with many
  *                 tokens (prefill, training);
@@ -194,6 +216,17 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  * With flags 0 the library picks weight tiles when M_total <= 64 * G (at most 64 tokens
  * per expert on average), else row tiles.  The two tilings may differ in the last bits
  * of the FP32 accumulation (both are within the GEMM tolerance of the method).
+ * Fused activation quantization (MPQ_FUSE_QUANT_A; page 4, third paragraph: decoding;
+ * page 2, third paragraph after the title: the FP8 cast on the way into the GEMM): A is
+ * then BF16 [M_total, K] with lda >= K in elements (16-byte aligned rows), sA must be NULL
+ * and ldsa is ignored.  One launch quantizes every expert row 1x128 exactly as
+ * fp8_quant_tile_1x128 does (amax/448 scales, or power-of-2 with MPQ_POW2) into the
+ * handle's workspace (mpq_set_workspace, mpq_grouped_fused_workspace_bytes), then runs
+ * the weight-tile GEMM on those codes; the output equals fp8_quant_tile_1x128 followed by
+ * this call with MPQ_GROUPED_WEIGHT_TILES, bit for bit.  The launch is cooperative: all
+ * of its CTAs (one per SM) must be resident at once, so it fails with MPQ_ERR_CUDA when
+ * the cooperative launch is refused (e.g. other work occupies SMs).
+ * Returns MPQ_ERR_WORKSPACE without a workspace of sufficient size.
  * Requirements: 1 <= G <= 1024; N % 128 == 0; K % 128 == 0; alignment as for
  * fp8_gemm_blockscaled.
  */

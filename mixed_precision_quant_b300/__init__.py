@@ -24,10 +24,11 @@ FPROP, DGRAD, WGRAD = 0, 1, 2
 OUT_BF16, OUT_FP32 = 0, 1
 POW2 = 1
 GROUPED_ROW_TILES, GROUPED_WEIGHT_TILES = 2, 4
+FUSE_QUANT_A = 8
 
 _STATUS = {0: "ok", 1: "null pointer argument", 2: "invalid size or leading dimension",
            3: "misaligned pointer or stride", 4: "unsupported op, dtype or flags",
-           5: "CUDA call failed", 6: "device-side wait timed out"}
+           5: "CUDA call failed", 6: "device-side wait timed out", 7: "no workspace set, or too small"}
 
 
 class MPQError(RuntimeError):
@@ -56,6 +57,8 @@ def _load() -> ctypes.CDLL:
         "fp8_gemm_blockscaled": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
         "fp8_grouped_gemm_blockscaled": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, U32, P]),
         "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
+        "mpq_set_workspace": (INT, [P, P, ctypes.c_size_t]),
+        "mpq_grouped_fused_workspace_bytes": (INT, [I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -66,6 +69,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 _handles: dict = {}
+_workspaces: dict = {}   # device index -> torch uint8 buffer handed to mpq_set_workspace
 _hlock = threading.Lock()
 
 
@@ -194,9 +198,30 @@ def fp8_gemm_blockscaled(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Te
     return C
 
 
-def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor,
+def fused_workspace_bytes(M_total: int, K: int, G: int) -> int:
+    """Workspace bytes for ``fp8_grouped_gemm_blockscaled(..., fuse_quant=True)``."""
+    n = ctypes.c_size_t()
+    _check("mpq_grouped_fused_workspace_bytes", _lib.mpq_grouped_fused_workspace_bytes(M_total, K, G, ctypes.byref(n)))
+    return n.value
+
+
+def _ensure_workspace(device: torch.device, nbytes: int):
+    """Give the device's handle a workspace of at least ``nbytes`` (a torch buffer kept by
+    this module; the library itself allocates nothing)."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    h = _handle(device)
+    with _hlock:
+        buf = _workspaces.get(idx)
+        if buf is None or buf.numel() < nbytes:
+            torch.cuda.current_stream(device).synchronize()   # no call in flight still uses the old one
+            buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            _workspaces[idx] = buf
+            _check("mpq_set_workspace", _lib.mpq_set_workspace(h, _ptr(buf), buf.numel()))
+
+
+def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Optional[torch.Tensor], B: torch.Tensor,
                                  sB: torch.Tensor, *, out_dtype: int = OUT_BF16, C: Optional[torch.Tensor] = None,
-                                 tiles: str = "auto", stream=None):
+                                 tiles: str = "auto", fuse_quant: bool = False, pow2: bool = False, stream=None):
     """MoE grouped FP8 GEMM: rows ``[off[g], off[g+1])`` of ``A`` use expert ``g``'s weight.
 
     ``offsets`` int64 CUDA ``[G+1]``; ``A [M, K]`` codes, ``sA [K/128, M]``; ``B [G, N, K]`` codes;
@@ -207,7 +232,16 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: tor
     flags = {"auto": 0, "rows": GROUPED_ROW_TILES, "weights": GROUPED_WEIGHT_TILES}.get(tiles)
     if flags is None:
         raise ValueError("tiles: expected 'auto', 'rows' or 'weights'")
-    _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
+    if fuse_quant:
+        # A is BF16 [M, K], quantized 1x128 inside the launch (pow2: power-of-2 scales)
+        _cuda2d(A, torch.bfloat16, "A")
+        if sA is not None:
+            raise ValueError("sA must be None with fuse_quant=True")
+        flags |= FUSE_QUANT_A | (POW2 if pow2 else 0)
+    else:
+        if pow2:
+            raise ValueError("pow2 applies to fuse_quant=True only")
+        _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
     if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.dim() == 1 and offsets.is_contiguous()):
         raise TypeError("offsets: expected a contiguous 1-D int64 CUDA tensor")
     if not (B.is_cuda and B.dtype == torch.uint8 and B.dim() == 3 and B.is_contiguous()):
@@ -220,6 +254,8 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: tor
         raise ValueError("shape mismatch between offsets, A and B")
     dev = A.device
     C = _out(M, N, out_dtype, C, dev)
+    if fuse_quant:
+        _ensure_workspace(dev, fused_workspace_bytes(M, K, G))
     st = _lib.fp8_grouped_gemm_blockscaled(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(A), _ld(A), _ptr(sA),
                                            _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
                                            int(out_dtype), flags, _stream(dev, stream))

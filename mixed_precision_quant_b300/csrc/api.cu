@@ -15,6 +15,8 @@ struct mpq_handle_s {
     int *d_status;          // [0] code, [1] tag of the wait that gave up
     uint64_t timeout_ns;
     bool gemm_pair;         // GEMMs on CTA pairs (cta_group::2, 256 x 256 tiles)
+    void *workspace;        // caller-owned scratch (mpq_set_workspace), may be null
+    size_t workspace_bytes;
 };
 
 namespace {
@@ -130,6 +132,7 @@ const char *mpq_status_string(int s)
     case MPQ_ERR_UNSUPPORTED: return "unsupported op, dtype or flags";
     case MPQ_ERR_CUDA: return "CUDA call failed";
     case MPQ_ERR_TIMEOUT: return "device-side wait timed out";
+    case MPQ_ERR_WORKSPACE: return "no workspace set, or too small";
     default: return "unknown status";
     }
 }
@@ -155,6 +158,8 @@ mpq_status mpq_create(mpq_handle *out)
     }
     h->timeout_ns = kDefaultTimeoutNs;
     h->gemm_pair = true;
+    h->workspace = nullptr;
+    h->workspace_bytes = 0;
     *out = h;
     return MPQ_OK;
 }
@@ -182,6 +187,33 @@ mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable)
     if (h == nullptr)
         return MPQ_ERR_NULL;
     h->gemm_pair = enable != 0;
+    return MPQ_OK;
+}
+
+mpq_status mpq_set_workspace(mpq_handle h, void *ptr, size_t bytes)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if ((ptr == nullptr) != (bytes == 0))
+        return MPQ_ERR_NULL;
+    if (!aligned(ptr, 256))
+        return MPQ_ERR_ALIGN;
+    h->workspace = ptr;
+    h->workspace_bytes = bytes;
+    return MPQ_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+mpq_status mpq_grouped_fused_workspace_bytes(int64_t M_total, int64_t K, int64_t G, size_t *bytes)
+{
+    if (bytes == nullptr)
+        return MPQ_ERR_NULL;
+    if (M_total < 0 || K <= 0 || K % 128 != 0 || G < 1)
+        return MPQ_ERR_SHAPE;
+    *bytes = align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)) +
+             align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) * sizeof(float)) +
+             align256(static_cast<size_t>(G) * sizeof(int));
     return MPQ_OK;
 }
 
@@ -343,6 +375,62 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
                                       static_cast<cudaStream_t>(stream)));
 }
 
+// Grouped GEMM with fused 1x128 quantization of the BF16 activations (weight tiles).
+static mpq_status grouped_fused(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total, int64_t N,
+                                int64_t K, const uint8_t *A, int64_t lda, const float *sA, const uint8_t *B,
+                                int64_t ldb, const float *sB, int64_t ldsb, void *C, int64_t ldc, int out_dtype,
+                                uint32_t flags, void *stream)
+{
+    if ((flags & ~(MPQ_FUSE_QUANT_A | MPQ_POW2 | MPQ_GROUPED_WEIGHT_TILES)) != 0 || sA != nullptr)
+        return MPQ_ERR_UNSUPPORTED;
+    if (A == nullptr || B == nullptr || sB == nullptr || C == nullptr)
+        return MPQ_ERR_NULL;
+    if (out_dtype != MPQ_OUT_BF16 && out_dtype != MPQ_OUT_FP32)
+        return MPQ_ERR_UNSUPPORTED;
+    if (N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || lda < K || ldb < K || ldc < N || ldsb < K / 128)
+        return MPQ_ERR_SHAPE;
+    if (G < 1 || G > 1024 || M_total < 0 || M_total > (int64_t(1) << 31) || K > (int64_t(1) << 31) ||
+        G * N > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    const int64_t esz = out_dtype == MPQ_OUT_FP32 ? 4 : 2;
+    if (!aligned(A, 16) || lda % 8 != 0 || !aligned(B, 16) || ldb % 16 != 0 || !aligned(C, 16) ||
+        (ldc * esz) % 16 != 0 || !aligned(sB, 4) || !aligned(d_offsets, 8))
+        return MPQ_ERR_ALIGN;
+    if (M_total == 0)
+        return MPQ_OK;
+    size_t need = 0;
+    mpq_status st = mpq_grouped_fused_workspace_bytes(M_total, K, G, &need);
+    if (st != MPQ_OK)
+        return st;
+    if (h->workspace == nullptr || h->workspace_bytes < need)
+        return MPQ_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(h->workspace);
+    uint8_t *xq = ws;
+    float *sx = reinterpret_cast<float *>(ws + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
+    int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
+                                         align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
+                                                  sizeof(float)));
+    mpq::GemmArgs a{};
+    a.M = M_total; a.N = N; a.K = K;
+    a.sA = sx; a.ldsa = M_total;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
+    a.C = C; a.ldc = ldc;
+    a.offsets = d_offsets; a.G = static_cast<int>(G);
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tmX, tmW;
+    if ((st = encode_operand(&tmX, xq, M_total, K, K, mpq::decode_x_box_rows())) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmW, B, G * N, K, ldb, 128)) != MPQ_OK)
+        return st;
+    mpq::FuseArgs f{};
+    f.x = reinterpret_cast<const uint16_t *>(A);
+    f.ldx = lda;
+    f.xq = xq; f.sx = sx; f.ready = ready;
+    f.pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
+    return from_cuda(mpq::launch_decode(tmX, tmW, a, out_dtype == MPQ_OUT_FP32, &f, h->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
                                         int64_t N, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
                                         int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB,
@@ -351,6 +439,9 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
 {
     if (h == nullptr || d_offsets == nullptr)
         return MPQ_ERR_NULL;
+    if ((flags & MPQ_FUSE_QUANT_A) != 0)
+        return grouped_fused(h, G, d_offsets, M_total, N, K, A, lda, sA, B, ldb, sB, ldsb, C, ldc, out_dtype, flags,
+                             stream);
     if ((flags & ~(MPQ_GROUPED_ROW_TILES | MPQ_GROUPED_WEIGHT_TILES)) != 0 ||
         flags == (MPQ_GROUPED_ROW_TILES | MPQ_GROUPED_WEIGHT_TILES))
         return MPQ_ERR_UNSUPPORTED;
@@ -379,7 +470,7 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
             return st;
         if ((st = encode_operand(&tmB, B, G * N, K, ldb, 128)) != MPQ_OK)
             return st;
-        return from_cuda(mpq::launch_decode(tmA, tmB, a, out_dtype == MPQ_OUT_FP32, h->num_sms,
+        return from_cuda(mpq::launch_decode(tmA, tmB, a, out_dtype == MPQ_OUT_FP32, nullptr, h->num_sms,
                                             static_cast<cudaStream_t>(stream)));
     }
     if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)

@@ -33,10 +33,20 @@
 //               by the two warps of each lane quarter, two loads in flight), one FMA per
 //               element into FP32 registers, then direct stores of C (each warp writes 32
 //               consecutive features of a token row per instruction).
+// With fused activation quantization (page 2 "9 Amazing Deepseek Hacks", third
+// paragraph after the title: the pages wish the FP8 cast to happen on the way into the
+// GEMM), the launch runs in two phases.  Phase 1, all warps: the experts' BF16 token rows
+// are quantized 1x128 (the arithmetic of the standalone quantizer, bit for bit) into a
+// caller-provided workspace, 32 rows at a time; each finished block is published by a
+// fence and an atomic add to a per-expert ready count.  Phase 2 is the GEMM above, whose
+// token producer and scale loader first wait (bounded) until their expert's count is
+// complete.  Every CTA finishes its phase-1 share before it waits on anything, and the
+// launch is cooperative (all CTAs resident), so every wait is for work that is running.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
+#include "quant_device.cuh"
 
 namespace mpq {
 namespace {
@@ -78,6 +88,29 @@ struct Item {
     int nb;         // 128-row block of the expert's weight
 };
 
+// Wait until *count >= target (acquire at GPU scope), bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count(const int *count, int target, const WaitCtl &c, int tag)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+        if (v >= target)
+            return true;
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            if (c.status != nullptr && atomicCAS(c.status, 0, kStatusTimeout) == 0)
+                atomicExch(c.status + 1, tag);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
     const uint64_t t0 = globaltimer_ns();
@@ -87,9 +120,10 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-template <bool OUT_F32>
+template <bool OUT_F32, bool FUSE>
 __global__ void __launch_bounds__(kDThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p)
+    decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p,
+                  const FuseArgs f)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -188,6 +222,50 @@ __global__ void __launch_bounds__(kDThreads, 1)
     const uint32_t tmem_base = misc[0];
     const int T = gitem[G];
 
+    if (FUSE) {
+        // ------------------------------------------------------------ phase 1: quantize
+        // Blocks of 32 token rows over [goff[0], goff[G]); thread -> (row, 128-column group),
+        // consecutive threads on consecutive groups of a row (256 contiguous bytes each).
+        const int r_begin = goff[0], r_end = goff[G];
+        const int nblk = (r_end - r_begin + 31) / 32;
+        for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
+            const int r0 = r_begin + b * 32, r1 = r0 + 32 < r_end ? r0 + 32 : r_end;
+            const int ngroups = (r1 - r0) * KB;
+            for (int gi = threadIdx.x; gi < ngroups; gi += blockDim.x) {
+                const int r = r0 + gi / KB, kb = gi - (gi / KB) * KB;
+                const uint4 *src = reinterpret_cast<const uint4 *>(f.x + static_cast<int64_t>(r) * f.ldx + kb * DK);
+                uint32_t w[64];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const uint4 v = __ldg(src + q);
+                    w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+                }
+                uint4 out[8];
+                const float sc = quantize_group128(w, f.pow2 != 0, out);
+                uint4 *dst = reinterpret_cast<uint4 *>(f.xq + static_cast<int64_t>(r) * p.K + kb * DK);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = out[q];
+                f.sx[static_cast<int64_t>(kb) * M + r] = sc;
+            }
+            fence_proxy_async_global();   // the codes are read by TMA (async proxy)
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int lo = 0, hi = G - 1;   // first expert whose rows end after r0
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (goff[mid + 1] > r0) hi = mid; else lo = mid + 1;
+                }
+                for (int g = lo; g < G && goff[g] < r1; ++g) {
+                    const int a = goff[g] > r0 ? goff[g] : r0, e = goff[g + 1] < r1 ? goff[g + 1] : r1;
+                    if (e > a)
+                        atomicAdd(f.ready + g, e - a);
+                }
+            }
+        }
+    }
+
     // Item t: expert g (last with gitem[g] <= t), then weight block fastest so that
     // neighbouring CTAs share the expert's tokens in L2 while streaming different weights.
     auto item_of = [&](int t) -> Item {
@@ -235,6 +313,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
             for (int t = blockIdx.x; t < T; t += gridDim.x) {
                 const Item ti = item_of(t);
                 const int nbox = (ti.ntok + kXBoxRows - 1) / kXBoxRows;
+                if (FUSE) {   // the expert's token codes are complete (phase 1 of all CTAs)
+                    if (!wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0590))
+                        goto xproducer_done;
+                    fence_proxy_async_global();
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % XSTAGES;
                     if (it >= static_cast<uint32_t>(XSTAGES)) {   // slice it - XSTAGES is done
@@ -295,6 +378,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 const Item ti = item_of(t);
                 const float *sw = p.sB + static_cast<int64_t>(ti.g) * p.sb_group_stride +
                                   static_cast<int64_t>(ti.nb) * p.ldsb;
+                if (FUSE && !wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0790))
+                    goto scale_done;
                 float px[SPF][DTOK / 32], pw[SPF];
                 auto fetch = [&](int kb, float (&x)[DTOK / 32], float &w) {
                     if (kb < KB) {
@@ -439,7 +524,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
 int decode_x_box_rows() { return kXBoxRows; }
 
 cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &a, bool out_fp32,
-                          int num_sms, cudaStream_t st)
+                          const FuseArgs *fuse, int num_sms, cudaStream_t st)
 {
     if (a.G > kDMaxGroups)
         return cudaErrorInvalidValue;
@@ -447,18 +532,41 @@ cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const 
     const int64_t items = ((a.M + DTOK - 1) / DTOK + a.G) * (a.N / 128);
     if (items <= 0)
         return cudaSuccess;
-    const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-    auto kern = out_fp32 ? decode_kernel<true> : decode_kernel<false>;
-    static bool configured[2] = {false, false};
-    if (!configured[out_fp32 ? 1 : 0]) {
+    // the fused form quantizes on every SM first, so it always takes one CTA per SM
+    const int grid = fuse != nullptr ? num_sms : static_cast<int>(items < num_sms ? items : num_sms);
+    const int ki = (out_fp32 ? 1 : 0) + (fuse != nullptr ? 2 : 0);
+    void (*kern)(CUtensorMap, CUtensorMap, GemmArgs, FuseArgs) =
+        ki == 0 ? decode_kernel<false, false> : ki == 1 ? decode_kernel<true, false>
+                : ki == 2 ? decode_kernel<false, true> : decode_kernel<true, true>;
+    static bool configured[4] = {false, false, false, false};
+    if (!configured[ki]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kDSmem));
         if (e != cudaSuccess)
             return e;
-        configured[out_fp32 ? 1 : 0] = true;
+        configured[ki] = true;
     }
-    kern<<<grid, kDThreads, kDSmem, st>>>(tmX, tmW, a);
-    return cudaGetLastError();
+    const FuseArgs none{};
+    if (fuse == nullptr) {
+        kern<<<grid, kDThreads, kDSmem, st>>>(tmX, tmW, a, none);
+        return cudaGetLastError();
+    }
+    // Phase 2 waits on phase-1 work of every CTA: a cooperative launch guarantees that all
+    // CTAs are resident at once (or the launch fails).
+    cudaError_t e = cudaMemsetAsync(fuse->ready, 0, sizeof(int) * static_cast<size_t>(a.G), st);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kDThreads, 1, 1);
+    cfg.dynamicSmemBytes = kDSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a, *fuse);
 }
 
 } // namespace mpq

@@ -64,9 +64,21 @@ int gemm_b_box_rows(bool pair);
 // tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
 // weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
 // the grouped launch_gemm (sB block scales [G][N/128][ldsb]); C is written directly.
+// Fused activation quantization: the token rows come as BF16 x [M, K] (ldx elements) and
+// are quantized 1x128 into the workspace (xq [M, K] codes, sx [K/128][M] scales, ready[G]
+// counts, cleared by the launcher) inside the same launch; tmX must then cover xq and
+// GemmArgs.sA / ldsa must be sx / M.
+struct FuseArgs {
+    const uint16_t *x;
+    int64_t ldx;
+    uint8_t *xq;
+    float *sx;
+    int *ready;
+    int pow2;
+};
 int decode_x_box_rows();
 cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &a, bool out_fp32,
-                          int num_sms, cudaStream_t st);
+                          const FuseArgs *fuse, int num_sms, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);
 

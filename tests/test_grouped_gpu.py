@@ -1,4 +1,6 @@
 """GPU parity of the grouped (MoE expert) block-scaled FP8 GEMM against the FP64 oracle."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -134,3 +136,102 @@ def test_moe_decode_full_size_sampled(mpq, tiles):
     d = workloads.moe_decode(device="cuda")
     _sampled_moe_check(mpq, d, "up", False, tiles)
     _sampled_moe_check(mpq, d, "down", True, tiles)
+
+
+# ------------------------------------------------- fused activation quantization (decode)
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("counts,lead,trail", [
+    ([3, 0, 130, 1, 200], 0, 0),
+    ([0, 0, 0, 257], 5, 7),
+    ([1] * 40, 3, 0),
+    ([256, 17, 64], 0, 9),
+])
+def test_fused_quant_equals_two_steps(mpq, counts, lead, trail, pow2):
+    """One fused launch == 1x128 quantizer then the weight-tile GEMM, bit for bit, and the
+    workspace holds exactly the standalone quantizer's codes and scales."""
+    G, N, K = len(counts), 256, 384
+    off = np.concatenate([[0], np.cumsum(counts)]) + lead
+    M = int(off[-1]) + trail
+    g = torch.Generator().manual_seed(1000 + sum(counts))
+    x = (torch.randn((M, K), generator=g) * 2).to(torch.bfloat16).cuda()
+    qb, sb = _experts(G, N, K, 21 + G)
+    offs = _dev(off.astype(np.int64))
+    qbd, sbd = _dev(qb), _dev(sb)
+    qx, sx, _, _ = mpq.fp8_quant_tile_1x128(x, pow2=pow2)
+    C2 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
+    mpq.fp8_grouped_gemm_blockscaled(offs, qx, sx, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C2, tiles="weights")
+    C1 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
+    mpq.fp8_grouped_gemm_blockscaled(offs, x, None, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C1, fuse_quant=True,
+                                     pow2=pow2)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    ws = mpq._workspaces[torch.cuda.current_device()]
+    r0, r1 = int(off[0]), int(off[-1])
+    codes = ws[:M * K].view(M, K)
+    assert torch.equal(codes[r0:r1], qx[r0:r1])
+    sx_off = (M * K + 255) // 256 * 256
+    scales = ws[sx_off:sx_off + (K // 128) * M * 4].view(torch.float32).view(K // 128, M)
+    assert torch.equal(scales[:, r0:r1].view(torch.int32), sx[:, r0:r1].view(torch.int32))
+    ref, absref = oracle.grouped_gemm_ref(off, *oracle.quant_tile_1x128(bf16_bits(x.cpu()), pow2=pow2), qb, sb)
+    rows = np.zeros(M, bool)
+    rows[r0:r1] = True
+    got = C1.cpu().numpy().astype(np.float64)
+    assert_gemm_close(got[rows], ref[rows], absref[rows], "fused")
+    assert np.all(got[~rows] == 777.0), "rows outside every expert were written"
+
+
+def test_moe_decode_fused_full_size_sampled(mpq):
+    """The decode workload end to end in one launch per projection: BF16 token rows in,
+    sampled outputs against the oracle (1x128 quantization of the same rows, FP64 GEMM)."""
+    d = workloads.moe_decode(device="cuda")
+    off = d["offsets"]
+    for proj, pow2 in (("up", False), ("down", True)):
+        X = d["X_up"] if proj == "up" else d["X_dn"]
+        Wt = d["W_up"] if proj == "up" else d["W_dn"]
+        G, N, K = Wt.shape
+        qw = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+        sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+        for e in range(G):
+            mpq.fp8_quant_block_128x128(Wt[e], q=qw[e], s=sw[e])
+        C = mpq.fp8_grouped_gemm_blockscaled(off.cuda(), X, None, qw, sw, fuse_quant=True, pow2=pow2)
+        torch.cuda.synchronize()
+        assert mpq.mpq_check_device_status() == (0, 0)
+        counts = d["counts"].numpy()
+        rng = np.random.default_rng(7)
+        for e in (int(np.argmax(counts)), int(np.argmin(counts)), int(rng.integers(0, G))):
+            r0, r1 = int(off[e]), int(off[e + 1])
+            rows = np.unique(np.concatenate([rng.integers(r0, r1, 8), [r0, r1 - 1]]))
+            oq, os_ = oracle.quant_tile_1x128(bf16_bits(X[torch.from_numpy(rows).cuda()]), pow2=pow2)
+            nb = int(rng.integers(0, N // 128))
+            oqw, _, osw = oracle.quant_block_128x128(bf16_bits(Wt[e, nb * 128:(nb + 1) * 128]))
+            ref, absref = oracle.gemm_ref(oracle.FPROP, oq, os_, oqw, osw)
+            got = C[torch.from_numpy(rows).cuda(), nb * 128:(nb + 1) * 128].float().cpu().numpy().astype(np.float64)
+            assert_gemm_close(got, ref, absref, f"fused {proj} expert {e}")
+
+
+def test_fused_quant_validation(mpq):
+    G, N, K, M = 2, 128, 256, 64
+    off = torch.tensor([0, 30, 64], dtype=torch.int64, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    qb = torch.zeros((G, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.ones((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        mpq.fp8_grouped_gemm_blockscaled(off, x, torch.ones((K // 128, M), device="cuda"), qb, sb, fuse_quant=True)
+    lib, h = mpq._lib, mpq._handle(x.device)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = lambda flags: (h, G, mpq._ptr(off), M, N, K, mpq._ptr(x), K, None, 0, mpq._ptr(qb), K, mpq._ptr(sb),
+                          K // 128, mpq._ptr(C), N, mpq.OUT_BF16, flags, s)
+    # rows tiles cannot fuse; no or too small a workspace is reported, not a fault
+    assert lib.fp8_grouped_gemm_blockscaled(*args(mpq.FUSE_QUANT_A | mpq.GROUPED_ROW_TILES)) == 4
+    mpq._workspaces.pop(torch.cuda.current_device(), None)
+    assert lib.mpq_set_workspace(h, None, 0) == 0
+    assert lib.fp8_grouped_gemm_blockscaled(*args(mpq.FUSE_QUANT_A)) == 7
+    small = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    assert lib.mpq_set_workspace(h, mpq._ptr(small), small.numel()) == 0
+    assert lib.fp8_grouped_gemm_blockscaled(*args(mpq.FUSE_QUANT_A)) == 7
+    assert lib.mpq_set_workspace(h, ctypes.c_void_p(small.data_ptr() + 16), 1024) == 3
+    assert lib.mpq_set_workspace(h, None, 0) == 0
+    n = mpq.fused_workspace_bytes(M, K, G)
+    assert n == (M * K + 255) // 256 * 256 + ((K // 128) * M * 4 + 255) // 256 * 256 + 256
