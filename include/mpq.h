@@ -238,6 +238,42 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
                                         void *stream);
 
 /*
+ * fp8_grouped_gemm_fused_quant_noalloc -- fp8_grouped_gemm_blockscaled with
+ * MPQ_FUSE_QUANT_A (fused 1x128 quantization of BF16 token rows, weight-tile GEMM) that
+ * allocates no memory and needs no workspace.  The source pages have no counterpart; it
+ * exists for callers that must not allocate device memory, or hand the library a
+ * buffer, while they run -- e.g. a serving process that reserves all device memory at
+ * start-up, or a latency-critical loop where an allocation (and the synchronisation it
+ * can bring) is not acceptable.
+ *
+ * The quantized activations live in a fixed scratch area inside the library's device
+ * code: MPQ_NOALLOC_SCRATCH_BYTES (64 MiB).  A call whose
+ * mpq_grouped_fused_workspace_bytes(M_total, K, G) exceeds it is rejected with
+ * MPQ_ERR_WORKSPACE before any launch (e.g. with K = 7168, up to about 9,000 token rows).
+ *
+ *   X       BF16 [M_total, K], ldx >= K elements, 16-byte aligned rows.
+ *   flags   0 or MPQ_POW2 (power-of-2 activation scales).
+ *   the other arguments as for fp8_grouped_gemm_blockscaled.
+ * Results equal fp8_grouped_gemm_blockscaled with MPQ_FUSE_QUANT_A bit for bit.
+ *
+ * First call: the first call on each device (with that device current) looks up the
+ * scratch area's address (cudaGetSymbolAddress, which may load the library's device code)
+ * and caches it; make that first call before any stream capture.
+ * Concurrency: there is one scratch area per device.  Calls that overlap in time -- on
+ * different streams, or from several threads, including through several handles -- race
+ * on it and corrupt each other's results; serialise them (calls on one stream are fine).
+ * The per-expert counters in the scratch area are cleared on the call's stream before
+ * the launch.
+ */
+#define MPQ_NOALLOC_SCRATCH_BYTES (64u << 20)
+mpq_status fp8_grouped_gemm_fused_quant_noalloc(mpq_handle h, int64_t G, const int64_t *d_offsets,
+                                                int64_t M_total, int64_t N, int64_t K,
+                                                const void *X, int64_t ldx,
+                                                const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                                void *C, int64_t ldc, int out_dtype, uint32_t flags,
+                                                void *stream);
+
+/*
  * mpq_selftest_wait_timeout -- launches one CTA that waits on a barrier nothing ever
  * arrives on, with the library's bounded wait and the given limit (nanoseconds).  The
  * wait must give up and record MPQ_ERR_TIMEOUT in the handle's status word; the

@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
         "mpq_set_workspace": (INT, [P, P, ctypes.c_size_t]),
         "mpq_grouped_fused_workspace_bytes": (INT, [I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
+        "fp8_grouped_gemm_fused_quant_noalloc": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, INT, U32, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -260,6 +261,34 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
                                            _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
                                            int(out_dtype), flags, _stream(dev, stream))
     _check("fp8_grouped_gemm_blockscaled", st)
+    return C
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def fp8_grouped_gemm_fused_quant_noalloc(offsets: torch.Tensor, X: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
+                                         C: torch.Tensor, *, out_dtype: int = OUT_BF16, pow2: bool = False,
+                                         stream=None):
+    """Fused 1x128 quantization + grouped weight-tile GEMM that allocates nothing: the
+    quantized activations stay in the library's fixed scratch area (NOALLOC_SCRATCH_BYTES),
+    so the output ``C`` must be given.  For callers that must not allocate device memory
+    while they run.  Calls that overlap in time (other streams or threads) race on the one
+    scratch area; the first call per device should come before any stream capture."""
+    _cuda2d(X, torch.bfloat16, "X")
+    if not (B.is_cuda and B.dtype == torch.uint8 and B.dim() == 3 and B.is_contiguous()):
+        raise TypeError("B: expected a contiguous [G, N, K] uint8 CUDA tensor")
+    if not (sB.is_cuda and sB.dtype == torch.float32 and sB.dim() == 3 and sB.is_contiguous()):
+        raise TypeError("sB: expected a contiguous [G, N/128, K/128] float32 CUDA tensor")
+    G, N, K = B.shape
+    M = X.shape[0]
+    if offsets.numel() != G + 1 or X.shape[1] != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch between offsets, X, B and C")
+    dev = X.device
+    st = _lib.fp8_grouped_gemm_fused_quant_noalloc(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(X), _ld(X), _ptr(B),
+                                                   K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C), int(out_dtype),
+                                                   POW2 if pow2 else 0, _stream(dev, stream))
+    _check("fp8_grouped_gemm_fused_quant_noalloc", st)
     return C
 
 

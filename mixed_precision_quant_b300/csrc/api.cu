@@ -431,6 +431,64 @@ static mpq_status grouped_fused(mpq_handle h, int64_t G, const int64_t *d_offset
                                         static_cast<cudaStream_t>(stream)));
 }
 
+// The allocation-free form of the fused grouped GEMM: the same validation and launch as
+// grouped_fused, with the library's fixed scratch area (noalloc.cu) as the workspace.
+mpq_status fp8_grouped_gemm_fused_quant_noalloc(mpq_handle h, int64_t G, const int64_t *d_offsets,
+                                                int64_t M_total, int64_t N, int64_t K, const void *X, int64_t ldx,
+                                                const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                                void *C, int64_t ldc, int out_dtype, uint32_t flags, void *stream)
+{
+    static_assert(mpq::kNoallocScratchBytes == MPQ_NOALLOC_SCRATCH_BYTES, "scratch size");
+    if (h == nullptr || d_offsets == nullptr || X == nullptr || B == nullptr || sB == nullptr || C == nullptr)
+        return MPQ_ERR_NULL;
+    if ((flags & ~MPQ_POW2) != 0 || (out_dtype != MPQ_OUT_BF16 && out_dtype != MPQ_OUT_FP32))
+        return MPQ_ERR_UNSUPPORTED;
+    if (N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldx < K || ldb < K || ldc < N || ldsb < K / 128)
+        return MPQ_ERR_SHAPE;
+    if (G < 1 || G > 1024 || M_total < 0 || M_total > (int64_t(1) << 31) || K > (int64_t(1) << 31) ||
+        G * N > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    const int64_t esz = out_dtype == MPQ_OUT_FP32 ? 4 : 2;
+    if (!aligned(X, 16) || ldx % 8 != 0 || !aligned(B, 16) || ldb % 16 != 0 || !aligned(C, 16) ||
+        (ldc * esz) % 16 != 0 || !aligned(sB, 4) || !aligned(d_offsets, 8))
+        return MPQ_ERR_ALIGN;
+    size_t need = 0;
+    mpq_status st = mpq_grouped_fused_workspace_bytes(M_total, K, G, &need);
+    if (st != MPQ_OK)
+        return st;
+    if (need > mpq::kNoallocScratchBytes)
+        return MPQ_ERR_WORKSPACE;
+    if (M_total == 0)
+        return MPQ_OK;
+    void *scratch = nullptr;
+    if (mpq::noalloc_scratch(&scratch) != cudaSuccess)
+        return MPQ_ERR_CUDA;
+    uint8_t *xq = static_cast<uint8_t *>(scratch);
+    float *sx = reinterpret_cast<float *>(xq + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
+    int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
+                                         align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
+                                                  sizeof(float)));
+    mpq::GemmArgs a{};
+    a.M = M_total; a.N = N; a.K = K;
+    a.sA = sx; a.ldsa = M_total;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
+    a.C = C; a.ldc = ldc;
+    a.offsets = d_offsets; a.G = static_cast<int>(G);
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tmX, tmW;
+    if ((st = encode_operand(&tmX, xq, M_total, K, K, mpq::decode_x_box_rows())) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmW, B, G * N, K, ldb, 128)) != MPQ_OK)
+        return st;
+    mpq::FuseArgs f{};
+    f.x = static_cast<const uint16_t *>(X);
+    f.ldx = ldx;
+    f.xq = xq; f.sx = sx; f.ready = ready;
+    f.pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
+    return from_cuda(mpq::launch_decode(tmX, tmW, a, out_dtype == MPQ_OUT_FP32, &f, h->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
                                         int64_t N, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
                                         int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB,

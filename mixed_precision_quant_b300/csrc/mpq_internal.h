@@ -76,6 +76,11 @@ struct FuseArgs {
     int *ready;
     int pow2;
 };
+// Size of the fixed scratch area of fp8_grouped_gemm_fused_quant_noalloc (MPQ_NOALLOC_SCRATCH_BYTES),
+// and its device address on the current device (looked up on first use, then cached).
+constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
+cudaError_t noalloc_scratch(void **ptr);
+
 int decode_x_box_rows();
 cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &a, bool out_fp32,
                           const FuseArgs *fuse, int num_sms, cudaStream_t st);
