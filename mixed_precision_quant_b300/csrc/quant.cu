@@ -14,10 +14,11 @@
 // 256 rows x 128 columns of BF16 (64 KB):
 //   * one producer warp loads a tile as four 128-row x 64-column TMA boxes with 128-byte
 //     swizzle into a shared-memory ring (completion counted on mbarriers);
-//   * eight consumer warps own one row each per thread (row groups) or one column group
-//     each per thread (column groups): a thread reads its 128 values with conflict-free
-//     16-byte (or 2-byte) shared loads, reduces the max-abs itself, derives the scale once
-//     and converts with the exact arithmetic of mpq_device.cuh;
+//   * consumer warps own one row group per thread (rows, blocks: eight warps) or half a
+//     row group and half a column group per thread (dual: sixteen warps, the halves'
+//     max-abs values meeting in one shuffle): a thread reads its values with 16-byte (or,
+//     down a column, 2-byte) shared loads, reduces the max-abs, derives the scale and
+//     converts with the exact arithmetic of quant_device.cuh;
 //   * codes are written into 128-byte-swizzled staging tiles, one per warpgroup, and
 //     leave with TMA bulk-tensor stores (coalesced, clipped at the tensor bounds).
 // Every wait is bounded.
@@ -166,19 +167,6 @@ __device__ __forceinline__ void load_row(uint32_t tile, int r, uint32_t (&w)[64]
         }
 }
 
-// Column c (0..127) of the tile over rows rh*128 .. +127: 64 words, word i = rows (2i, 2i+1).
-__device__ __forceinline__ void load_col(uint32_t tile, int c, int rh, uint32_t (&w)[64])
-{
-    const uint32_t box = tile + (rh * 2 + (c >> 6)) * kBox;
-    const int j = (c & 63) >> 3, e = (c & 7) << 1;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-        const uint32_t lo = lds_u16(box + sw128(2 * i, j) + e);
-        const uint32_t hi = lds_u16(box + sw128(2 * i + 1, j) + e);
-        w[i] = lo | (hi << 16);
-    }
-}
-
 // 128 values (64 words) -> 8 code chunks written to row `r` of a swizzled staging box.
 __device__ __forceinline__ void write_codes(uint32_t box, int r, const uint32_t (&w)[64], const GroupScale &g)
 {
@@ -247,65 +235,108 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // --------------------------------------------------- fused 1x128 + 128x1 (dual)
-//
-// Row groups as in the row kernel; then thread t owns column t % 128 over the 128 rows of
-// warpgroup half t / 128 (one 128x1 group) and writes its codes as row (t % 128) of the
-// transposed staging box of that half.
 constexpr int QD_STAGES = 2;
 
+// ------------------------------------------- fused 1x128 + 128x1, sixteen warps
+//
+// Row groups as in the row kernel, plus the 128x1 column groups written transposed (one
+// read of the tile for both).  One thread per group would need 64 words of data in
+// registers, which leaves room for eight consumer warps only, too few to hide the
+// latencies of a pass (shared loads, the max-abs tree, the scale's division).  Here each
+// thread owns half a group -- 64 values -- and the two halves' max-abs values meet in one
+// shuffle, so sixteen consumer warps fit.  Warps 8h .. 8h+7 own rows 128h .. +127 of the
+// tile; within them thread u (0..255) holds
+//   row pass:    row u/2, columns 64 (u%2) .. +63;
+//   column pass: column u/2, rows 64 (u%2) .. +63 of the half.
+constexpr int kDualConsumers = 16;
+constexpr int kDualThreads = 32 * (kDualConsumers + 1);
+
 template <bool POW2, bool ROWS>
-__global__ void __launch_bounds__(kQThreads, 1)
-    quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
-                      const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
+__global__ void __launch_bounds__(kDualThreads, 1)
+    quant_dual16_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
+                        const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
     const QSmem sm = q_carve<QD_STAGES, true>(smem_raw);
-    q_init<QD_STAGES>(sm);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QD_STAGES; ++i) {
+            mbar_init(sm.bars + 8 * i, 1);
+            mbar_init(sm.bars + 8 * (QD_STAGES + i), kDualConsumers);
+        }
+        mbar_init(sm.bars + 8 * (2 * QD_STAGES), 8);
+        mbar_init(sm.bars + 8 * (2 * QD_STAGES + 1), 8);
+        *sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
     const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
     const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
-    if (warp == kConsumers) {
+    if (warp == kDualConsumers) {
         if (lane == 0)
             q_produce<QD_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
         return;
     }
-    const int h = t >> 7, rr = t & 127;
+    const int h = t >> 8, u = t & 255;
+    const int g2 = u >> 1, sub = u & 1;                    // group (row or column) and half
     const uint32_t wgbar = sm.bars + 8 * (2 * QD_STAGES + h);
     const uint32_t out_r = sm.out_rows + h * kBox, out_c = sm.out_cols + h * kBox;
-    const bool elected = rr == 0;
+    const bool elected = u == 0;
     uint32_t cph = 0, it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const uint32_t st = it % QD_STAGES, ph = (it / QD_STAGES) & 1;
-        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1300 | st))
+        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1500 | st))
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
         const uint32_t tile = sm.stage + st * kTile;
-        const int64_t y = rb * kTileRows + h * 128;       // first row of this warpgroup's half
+        const int64_t y = rb * kTileRows + h * 128;       // first row of this half
         const bool half_in = y < p.rows;                   // rows is a multiple of 128
         if (elected)
             bulk_wait_read0();                             // both staging boxes are free
-        if (!wg_sync(wgbar, cph, ctl, 0x1310))
+        if (!wg_sync(wgbar, cph, ctl, 0x1510))
             break;
-        uint32_t w[64];
+        uint32_t w[32];
         if (ROWS) {
-            load_row(tile, t, w);
-            const GroupScale g = make_group_scale(amax_words(w), POW2);
-            if (half_in)
-                p.s[cb * p.lds + y + rr] = g.s;
-            write_codes(out_r, rr, w, g);
+            const uint32_t box = tile + (h * 2 + sub) * kBox;   // rows of this half, columns 64 sub ..
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 v = lds_v4(box + sw128(g2, j));
+                w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+            }
+            float a = amax_words(w);
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            const GroupScale g = make_group_scale(a, POW2);
+            if (half_in && sub == 0)
+                p.s[cb * p.lds + y + g2] = g.s;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                sts_v4(out_r + sw128(g2, sub * 4 + q), codes16(&w[q * 8], g));
         }
-        load_col(tile, rr, h, w);
+        {
+            const uint32_t box = tile + (h * 2 + (g2 >> 6)) * kBox;
+            const int j = (g2 & 63) >> 3, e = (g2 & 7) << 1;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t lo = lds_u16(box + sw128(64 * sub + 2 * i, j) + e);
+                const uint32_t hi = lds_u16(box + sw128(64 * sub + 2 * i + 1, j) + e);
+                w[i] = lo | (hi << 16);
+            }
+        }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(sm.bars + 8 * (QD_STAGES + st));   // this warp has read the tile
         {
-            const GroupScale g = make_group_scale(amax_words(w), POW2);
-            if (half_in)
-                p.sT[(y / 128) * p.ldsT + cb * 128 + rr] = g.s;
-            write_codes(out_c, rr, w, g);
+            float a = amax_words(w);
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            const GroupScale g = make_group_scale(a, POW2);
+            if (half_in && sub == 0)
+                p.sT[(y / 128) * p.ldsT + cb * 128 + g2] = g.s;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                sts_v4(out_c + sw128(g2, sub * 4 + q), codes16(&w[q * 8], g));
         }
         fence_proxy_async_smem();
-        if (!wg_sync(wgbar, cph, ctl, 0x1311))
+        if (!wg_sync(wgbar, cph, ctl, 0x1511))
             break;
         if (elected && half_in) {
             if (ROWS)
@@ -405,13 +436,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 template <class K, class... Args>
-cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream_t st, Args... args)
+cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream_t st, int threads, Args... args)
 {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int64_t grid = items < num_sms ? items : num_sms;
-    kern<<<static_cast<int>(grid), kQThreads, smem, st>>>(args...);
+    kern<<<static_cast<int>(grid), threads, smem, st>>>(args...);
     return cudaGetLastError();
 }
 
@@ -424,8 +455,8 @@ cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, co
     if (items == 0)
         return cudaSuccess;
     constexpr size_t smem = q_smem_bytes<QR_STAGES, false>();
-    return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, tmx, tmq, a)
-                : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, tmx, tmq, a);
+    return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, kQThreads, tmx, tmq, a)
+                : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, kQThreads, tmx, tmq, a);
 }
 
 cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
@@ -437,10 +468,14 @@ cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, co
     constexpr size_t smem = q_smem_bytes<QD_STAGES, true>();
     const bool rows_out = a.q != nullptr;
     if (pow2)
-        return rows_out ? launch_q(quant_dual_kernel<true, true>, smem, items, num_sms, st, tmx, tmq, tmqT, a)
-                        : launch_q(quant_dual_kernel<true, false>, smem, items, num_sms, st, tmx, tmq, tmqT, a);
-    return rows_out ? launch_q(quant_dual_kernel<false, true>, smem, items, num_sms, st, tmx, tmq, tmqT, a)
-                    : launch_q(quant_dual_kernel<false, false>, smem, items, num_sms, st, tmx, tmq, tmqT, a);
+        return rows_out ? launch_q(quant_dual16_kernel<true, true>, smem, items, num_sms, st, kDualThreads, tmx, tmq,
+                                   tmqT, a)
+                        : launch_q(quant_dual16_kernel<true, false>, smem, items, num_sms, st, kDualThreads, tmx, tmq,
+                                   tmqT, a);
+    return rows_out ? launch_q(quant_dual16_kernel<false, true>, smem, items, num_sms, st, kDualThreads, tmx, tmq,
+                               tmqT, a)
+                    : launch_q(quant_dual16_kernel<false, false>, smem, items, num_sms, st, kDualThreads, tmx, tmq,
+                               tmqT, a);
 }
 
 cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
@@ -453,10 +488,10 @@ cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, c
     constexpr size_t smem_t = q_smem_bytes<QB_STAGES, true>();
     constexpr size_t smem_n = q_smem_bytes<QB_STAGES, false>();
     if (pow2)
-        return tr ? launch_q(quant_block_kernel<true, true>, smem_t, items, num_sms, st, tmx, tmq, tmqT, a)
-                  : launch_q(quant_block_kernel<true, false>, smem_n, items, num_sms, st, tmx, tmq, tmqT, a);
-    return tr ? launch_q(quant_block_kernel<false, true>, smem_t, items, num_sms, st, tmx, tmq, tmqT, a)
-              : launch_q(quant_block_kernel<false, false>, smem_n, items, num_sms, st, tmx, tmq, tmqT, a);
+        return tr ? launch_q(quant_block_kernel<true, true>, smem_t, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a)
+                  : launch_q(quant_block_kernel<true, false>, smem_n, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a);
+    return tr ? launch_q(quant_block_kernel<false, true>, smem_t, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a)
+              : launch_q(quant_block_kernel<false, false>, smem_n, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a);
 }
 
 } // namespace mpq

@@ -11,19 +11,22 @@
 namespace mpq {
 
 // max |x| of the BF16 pairs in w[0..N), in packed BF16x2 arithmetic (exact), as binary32.
+// max.xorsign.abs compares magnitudes (its result's sign is the XOR of the operands'
+// signs, cleared once at the end), so no masking is needed per word.
 template <int N>
 __device__ __forceinline__ float amax_words(const uint32_t (&w)[N])
 {
     uint32_t m[N];
 #pragma unroll
     for (int i = 0; i < N; ++i)
-        m[i] = w[i] & 0x7FFF7FFFu;
+        m[i] = w[i];
 #pragma unroll
     for (int s = N / 2; s > 0; s >>= 1)
 #pragma unroll
         for (int i = 0; i < s; ++i)
-            asm("max.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[i]), "r"(m[i + s]));
-    return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xFFFF0000u));
+            asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[i]), "r"(m[i + s]));
+    const uint32_t a = m[0] & 0x7FFF7FFFu;
+    return fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
 }
 
 // Sixteen BF16 values (8 words, memory order) -> sixteen E4M3 codes (one 16-byte chunk),
