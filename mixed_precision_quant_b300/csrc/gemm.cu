@@ -306,33 +306,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ---------------------------------------------------------- MMA issuer
+            // One lane issues for the CTA (or the pair) and shares its SMSP with two busy
+            // promotion warps, so its loop is kept short: descriptors are a precomputed base
+            // plus a small offset (the 14-bit start-address field cannot carry: shared
+            // addresses stay below 2^18), and the ring positions advance incrementally.
             const uint32_t idesc = idesc_e4m3_f32(PAIR ? 256 : 128, BN);
-            uint32_t it = 0;
+            const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(smA));
+            const uint64_t db0 = sdesc_kmajor_sw128(smem_u32(smB));
+            uint32_t s = 0, ph = 0, buf = 0, tph = 0;
             for (int t = unit; t < T; t += nunits) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    const uint32_t buf = it & 1, tph = (it >> 1) & 1;
+                for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(bar(C::BAR_TEMPTY + buf), tph ^ 1, ctl, 0x0200 | buf))
                         goto mma_done;
                     if (!mbar_wait(bar(C::BAR_FULL + s), ph, ctl, 0x0210 | s))
                         goto mma_done;
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smA + s * A_BYTES);
-                    const uint32_t b0 = smem_u32(smB + s * C::B_BYTES);
+                    const uint64_t da = da0 + s * (A_BYTES >> 4), db = db0 + s * (C::B_BYTES >> 4);
                     const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
+                    for (int k = 0; k < BK / 32; ++k) {   // K = 32 per MMA: +32 bytes = +2 in the field
                         if (PAIR)
-                            umma_e4m3_pair(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
-                                           k > 0 ? 1u : 0u);
+                            umma_e4m3_pair(d, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
                         else
-                            umma_e4m3(d, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32), idesc,
-                                      k > 0 ? 1u : 0u);
+                            umma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0 ? 1u : 0u);
                     }
                     if (PAIR)
                         umma_commit_pair_mc(bar(C::BAR_DONE + s), 0x3);   // in both CTAs
                     else
                         umma_commit(bar(C::BAR_DONE + s));
+                    if (++s == static_cast<uint32_t>(STAGES)) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    buf ^= 1;
+                    tph ^= buf ^ 1;   // flips after every second slice
                 }
             }
         mma_done:
