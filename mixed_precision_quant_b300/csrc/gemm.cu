@@ -30,9 +30,9 @@
 //   warps 4-11  promotion: tcgen05.ld the slice partial (two loads in flight), multiply
 //               by its two scales and accumulate into FP32 registers with scalar FMAs;
 //               promotion of slice k overlaps the MMAs of slice k+1.  The finished tile is
-//               written as BF16 or FP32 through swizzled staging buffers (two of 2 KB per
-//               warp in pair mode, so one piece is filled while the previous one is stored)
-//               and TMA bulk-tensor stores (32 rows x 64 bytes per store).
+//               written as BF16 or FP32 through swizzled staging buffers (four of 2 KB per
+//               warp in pair mode, so the stores drain while the next tile starts) and TMA
+//               bulk-tensor stores (32 rows x 64 bytes per store).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
@@ -52,8 +52,11 @@ constexpr int kMaxGroups = 1024;
 
 template <bool PAIR>
 struct Cfg {
-    static constexpr int STAGES = PAIR ? 5 : 4;
-    static constexpr int OUT_BUFS = PAIR ? 2 : 1;             // staging buffers per promotion warp
+    static constexpr int STAGES = 4;
+    // Staging buffers per promotion warp: in pair mode four (8 KB, a whole warp tile in BF16),
+    // so a tile's TMA stores drain during the next tile's main loop instead of holding the
+    // warp back -- the output is written in a burst, when the write path is saturated.
+    static constexpr int OUT_BUFS = PAIR ? 4 : 1;
     static constexpr int B_ROWS = PAIR ? 128 : 256;          // B rows staged by one CTA per slice
     static constexpr uint32_t B_BYTES = B_ROWS * BK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -460,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ch = 0; ch < 128 / COLS; ++ch) {
                         const uint32_t stg_u32 = stg0 + (ch % C::OUT_BUFS) * STAGE_OUT;
                         if (lane == 0) {                                // the buffer's last piece has left smem
-                            if (C::OUT_BUFS == 2)
-                                bulk_wait_read1();
+                            if (C::OUT_BUFS == 4)
+                                bulk_wait_read3();
                             else
                                 bulk_wait_read0();
                         }
