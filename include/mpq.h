@@ -92,10 +92,15 @@ mpq_status mpq_destroy(mpq_handle h);
  * (default 1e9).  0 restores the default. */
 mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
 
-/* Data sharing of the GEMM entry points issued through this handle.  1 (default): CTAs
- * run as 2-CTA clusters on neighbouring SMs whose 128 x 256 output tiles share the same
- * B (weight) rows; each CTA loads half of the B slice and multicasts it to both.  0: every
- * CTA loads its own operands.  The results are bit-identical. */
+/* Tiling of the row-tiled GEMMs issued through this handle.
+ *   pair tiles: a 2-CTA cluster on two SMs computes a 256 x 256 tile with 2-SM MMAs (each
+ *     SM stages its 128 A rows and half of the B rows);
+ *   single-SM tiles: one CTA computes a 128 x 256 tile.
+ * mode 1 (default): pair tiles for fp8_gemm_blockscaled; for the row-tiled grouped GEMM
+ * pair tiles only when the experts average 2048 rows or more (each expert's rows are
+ * rounded up to whole tiles, and a 256-row tile wastes more), else single-SM tiles.
+ * mode 0: single-SM tiles everywhere.  mode 2: pair tiles everywhere.  Other values:
+ * MPQ_ERR_UNSUPPORTED.  The tilings give bit-identical results. */
 mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
 
 /*

@@ -307,10 +307,12 @@ def mpq_set_wait_timeout(timeout_ns: int, device=None):
     _check("mpq_set_wait_timeout", _lib.mpq_set_wait_timeout(_handle(dev), int(timeout_ns)))
 
 
-def mpq_set_gemm_cta_pair(enable: bool, device=None):
-    """Run GEMM tiles on SM pairs (True, default) or single SMs (False)."""
+def mpq_set_gemm_cta_pair(mode, device=None):
+    """Tiling of the row-tiled GEMMs: 1 or True (default) -- 2-SM pair tiles for dense GEMMs,
+    for grouped ones only when experts average 2048 rows or more; 0 or False -- single-SM
+    tiles everywhere; 2 -- pair tiles everywhere."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    _check("mpq_set_gemm_cta_pair", _lib.mpq_set_gemm_cta_pair(_handle(dev), int(bool(enable))))
+    _check("mpq_set_gemm_cta_pair", _lib.mpq_set_gemm_cta_pair(_handle(dev), int(mode)))
 
 
 def mpq_selftest_wait_timeout(timeout_ns: int = 1_000_000, device=None, stream=None):

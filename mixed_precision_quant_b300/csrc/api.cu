@@ -14,7 +14,7 @@ struct mpq_handle_s {
     int num_sms;
     int *d_status;          // [0] code, [1] tag of the wait that gave up
     uint64_t timeout_ns;
-    bool gemm_pair;         // GEMMs on CTA pairs (cta_group::2, 256 x 256 tiles)
+    int pair_mode;          // 2-SM pair tiles: 0 never, 1 dense (+ grouped with large experts), 2 always
     void *workspace;        // caller-owned scratch (mpq_set_workspace), may be null
     size_t workspace_bytes;
 };
@@ -157,7 +157,7 @@ mpq_status mpq_create(mpq_handle *out)
         return MPQ_ERR_CUDA;
     }
     h->timeout_ns = kDefaultTimeoutNs;
-    h->gemm_pair = true;
+    h->pair_mode = 1;
     h->workspace = nullptr;
     h->workspace_bytes = 0;
     *out = h;
@@ -186,7 +186,9 @@ mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable)
 {
     if (h == nullptr)
         return MPQ_ERR_NULL;
-    h->gemm_pair = enable != 0;
+    if (enable < 0 || enable > 2)
+        return MPQ_ERR_UNSUPPORTED;
+    h->pair_mode = enable;
     return MPQ_OK;
 }
 
@@ -358,7 +360,8 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     CUtensorMap tmA, tmB;
     if ((st = encode_operand(&tmA, A, M, K, lda, 128)) != MPQ_OK)
         return st;
-    if ((st = encode_operand(&tmB, B, N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
+    const bool pair = h->pair_mode != 0;
+    if ((st = encode_operand(&tmB, B, N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
         return st;
     CUtensorMap tmC;
     if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
@@ -371,7 +374,7 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     a.offsets = nullptr; a.G = 1;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
-    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, h->gemm_pair, h->num_sms,
+    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, pair, h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -533,12 +536,15 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     }
     if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
         return st;
-    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(h->gemm_pair))) != MPQ_OK)
+    // Pair tiles round every expert's rows up to 256, single-SM tiles to 128: by default the
+    // grouped GEMM takes pairs only for experts of 2048 rows or more on average.
+    const bool pair = h->pair_mode == 2 || (h->pair_mode == 1 && M_total >= 2048 * G);
+    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
         return st;
     CUtensorMap tmC;
     if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
         return st;
-    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, h->gemm_pair,
+    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, pair,
                                       h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }

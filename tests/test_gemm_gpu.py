@@ -27,9 +27,9 @@ def mpq():
 @pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
 def tiles(request, mpq):
     """Run the test with 256x256 tiles on SM pairs and with 128x256 tiles on single SMs."""
-    mpq.mpq_set_gemm_cta_pair(request.param)
+    mpq.mpq_set_gemm_cta_pair(2 if request.param else 0)
     yield request.param
-    mpq.mpq_set_gemm_cta_pair(True)
+    mpq.mpq_set_gemm_cta_pair(1)
 
 
 def _bf16(shape, std, seed, outliers=0.0):
@@ -123,6 +123,32 @@ def test_wgrad(mpq, tiles, T, Kin, Nout):
     C = mpq.fp8_gemm_blockscaled(mpq.WGRAD, _dev(qaT), _dev(saT), _dev(qbT), _dev(sbT), out_dtype=mpq.OUT_FP32)
     ref, absref = oracle.gemm_ref(oracle.WGRAD, qaT, saT, qbT, sbT)
     assert_gemm_close(_out_host(C), ref, absref, "wgrad")
+
+
+@pytest.mark.parametrize("op", ["fprop", "wgrad"])
+def test_pair_and_single_tiles_agree_bit_for_bit(mpq, op):
+    """2-SM pair tiles (M = 256 MMAs over two SMs) and single-SM tiles (M = 128) give the
+    same FP32 results, bit for bit."""
+    g = torch.Generator().manual_seed(17)
+    if op == "fprop":
+        a = _bf16((300, 640), 1.0, 5)
+        w = _bf16((384, 640), 0.02, 6)
+        qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
+        qb, _, sb = oracle.quant_block_128x128(bf16_bits(w))
+        args = (mpq.FPROP, _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    else:
+        x = _bf16((512, 384), 1.0, 7)
+        dy = workloads.student_t3((512, 256), 1e-3, g, "cpu")
+        qaT, saT = oracle.quant_tile_128x1(bf16_bits(x))
+        qbT, sbT = oracle.quant_tile_128x1(bf16_bits(dy), pow2=True)
+        args = (mpq.WGRAD, _dev(qaT), _dev(saT), _dev(qbT), _dev(sbT))
+    outs = []
+    for mode in (2, 0):
+        mpq.mpq_set_gemm_cta_pair(mode)
+        outs.append(mpq.fp8_gemm_blockscaled(*args, out_dtype=mpq.OUT_FP32))
+    mpq.mpq_set_gemm_cta_pair(1)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
 
 
 # ------------------------------------------------------------ full-size samples

@@ -24,7 +24,7 @@ def mpq():
 def tiles(request, mpq):
     """Run the test with token-row tiles (256x256 on SM pairs, 128x256 on single SMs) and
     with weight-row tiles sized to each expert's tokens; yields the `tiles` argument."""
-    mpq.mpq_set_gemm_cta_pair(request.param != "rows_single_sm")
+    mpq.mpq_set_gemm_cta_pair(0 if request.param == "rows_single_sm" else 2)
     yield "weights" if request.param == "weights" else "rows"
     mpq.mpq_set_gemm_cta_pair(True)
 
