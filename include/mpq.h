@@ -215,20 +215,20 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  *   row tiles     tiles of 256 (or 128) token rows x 256 features, for experts with many
  *                 tokens (prefill, training);
  *   weight tiles  one 128-row block of an expert's weight against all of the expert's
- *                 tokens (up to 256 per tile), the MMA sized to the token count: for the
- *                 few tokens per expert of decoding, where streaming the weights from
- *                 memory sets the pace.
- * With flags 0 the library picks weight tiles when M_total <= 64 * G (at most 64 tokens
- * per expert on average), else row tiles.  The two tilings may differ in the last bits
- * of the FP32 accumulation (both are within the GEMM tolerance of the method).
+ *                 tokens (up to 256 per tile), the MMA sized to the token count.
+ * With flags 0 the library takes row tiles: on single-SM tiles (see mpq_set_gemm_cta_pair)
+ * they stream the weights at the HBM rate even for a few tokens per expert, faster than
+ * weight tiles on this hardware.  The two tilings may differ in the last bits of the FP32
+ * accumulation (both are within the GEMM tolerance of the method).
  * Fused activation quantization (MPQ_FUSE_QUANT_A; page 4, third paragraph: decoding;
  * page 2, third paragraph after the title: the FP8 cast on the way into the GEMM): A is
  * then BF16 [M_total, K] with lda >= K in elements (16-byte aligned rows), sA must be NULL
  * and ldsa is ignored.  One launch quantizes every expert row 1x128 exactly as
  * fp8_quant_tile_1x128 does (amax/448 scales, or power-of-2 with MPQ_POW2) into the
  * handle's workspace (mpq_set_workspace, mpq_grouped_fused_workspace_bytes), then runs
- * the weight-tile GEMM on those codes; the output equals fp8_quant_tile_1x128 followed by
- * this call with MPQ_GROUPED_WEIGHT_TILES, bit for bit.  The launch is cooperative: all
+ * the row-tile GEMM (single-SM tiles) on those codes -- or the weight-tile GEMM with
+ * MPQ_GROUPED_WEIGHT_TILES; the output equals fp8_quant_tile_1x128 followed by this call
+ * on the same tiling, bit for bit.
  * of its CTAs (one per SM) must be resident at once, so it fails with MPQ_ERR_CUDA when
  * the cooperative launch is refused (e.g. other work occupies SMs).
  * Returns MPQ_ERR_WORKSPACE without a workspace of sufficient size.
@@ -244,7 +244,7 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
 
 /*
  * fp8_grouped_gemm_fused_quant_noalloc -- fp8_grouped_gemm_blockscaled with
- * MPQ_FUSE_QUANT_A (fused 1x128 quantization of BF16 token rows, weight-tile GEMM) that
+ * MPQ_FUSE_QUANT_A (fused 1x128 quantization of BF16 token rows, row-tile GEMM) that
  * allocates no memory and needs no workspace.  The source pages have no counterpart; it
  * exists for callers that must not allocate device memory, or hand the library a
  * buffer, while they run -- e.g. a serving process that reserves all device memory at

@@ -228,8 +228,8 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
     ``offsets`` int64 CUDA ``[G+1]``; ``A [M, K]`` codes, ``sA [K/128, M]``; ``B [G, N, K]`` codes;
     ``sB [G, N/128, K/128]``.  Rows outside every expert are left untouched in ``C``.
     ``tiles``: ``"rows"`` (token-row tiles, many tokens per expert), ``"weights"`` (weight-row
-    tiles sized to each expert's tokens, for decoding) or ``"auto"`` (weights when there are
-    at most 64 tokens per expert on average)."""
+    tiles sized to each expert's tokens) or ``"auto"`` (rows: on single-SM tiles they stream
+    the weights at the HBM rate even for a few tokens per expert)."""
     flags = {"auto": 0, "rows": GROUPED_ROW_TILES, "weights": GROUPED_WEIGHT_TILES}.get(tiles)
     if flags is None:
         raise ValueError("tiles: expected 'auto', 'rows' or 'weights'")

@@ -378,7 +378,53 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
                                       static_cast<cudaStream_t>(stream)));
 }
 
-// Grouped GEMM with fused 1x128 quantization of the BF16 activations (weight tiles).
+// Fused grouped GEMM after validation: carve the workspace (codes [M, K], scales [K/128][M],
+// per-expert counts) and launch on row tiles (single-SM, cooperative) or, with
+// MPQ_GROUPED_WEIGHT_TILES, on weight tiles.
+static mpq_status launch_fused_grouped(mpq_handle h, void *workspace, int64_t G, const int64_t *d_offsets,
+                                       int64_t M_total, int64_t N, int64_t K, const void *X, int64_t ldx,
+                                       const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb, void *C,
+                                       int64_t ldc, int out_dtype, uint32_t flags, void *stream)
+{
+    uint8_t *xq = static_cast<uint8_t *>(workspace);
+    float *sx = reinterpret_cast<float *>(xq + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
+    int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
+                                         align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
+                                                  sizeof(float)));
+    mpq::GemmArgs a{};
+    a.M = M_total; a.N = N; a.K = K;
+    a.sA = sx; a.ldsa = M_total;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
+    a.C = C; a.ldc = ldc;
+    a.offsets = d_offsets; a.G = static_cast<int>(G);
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    mpq::FuseArgs f{};
+    f.x = static_cast<const uint16_t *>(X);
+    f.ldx = ldx;
+    f.xq = xq; f.sx = sx; f.ready = ready;
+    f.pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
+    const bool fp32 = out_dtype == MPQ_OUT_FP32;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mpq_status e;
+    if ((flags & MPQ_GROUPED_WEIGHT_TILES) != 0) {
+        CUtensorMap tmX, tmW;
+        if ((e = encode_operand(&tmX, xq, M_total, K, K, mpq::decode_x_box_rows())) != MPQ_OK)
+            return e;
+        if ((e = encode_operand(&tmW, B, G * N, K, ldb, 128)) != MPQ_OK)
+            return e;
+        return from_cuda(mpq::launch_decode(tmX, tmW, a, fp32, &f, h->num_sms, st));
+    }
+    CUtensorMap tmA, tmB, tmC;
+    if ((e = encode_operand(&tmA, xq, M_total, K, K, 128)) != MPQ_OK)
+        return e;
+    if ((e = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(false))) != MPQ_OK)
+        return e;
+    if ((e = encode_output(&tmC, C, M_total, N, ldc, fp32)) != MPQ_OK)
+        return e;
+    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, fp32, false, h->num_sms, st, &f));
+}
+
+// Grouped GEMM with fused 1x128 quantization of the BF16 activations.
 static mpq_status grouped_fused(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total, int64_t N,
                                 int64_t K, const uint8_t *A, int64_t lda, const float *sA, const uint8_t *B,
                                 int64_t ldb, const float *sB, int64_t ldsb, void *C, int64_t ldc, int out_dtype,
@@ -407,31 +453,8 @@ static mpq_status grouped_fused(mpq_handle h, int64_t G, const int64_t *d_offset
         return st;
     if (h->workspace == nullptr || h->workspace_bytes < need)
         return MPQ_ERR_WORKSPACE;
-    uint8_t *ws = static_cast<uint8_t *>(h->workspace);
-    uint8_t *xq = ws;
-    float *sx = reinterpret_cast<float *>(ws + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
-    int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
-                                         align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
-                                                  sizeof(float)));
-    mpq::GemmArgs a{};
-    a.M = M_total; a.N = N; a.K = K;
-    a.sA = sx; a.ldsa = M_total;
-    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
-    a.C = C; a.ldc = ldc;
-    a.offsets = d_offsets; a.G = static_cast<int>(G);
-    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    CUtensorMap tmX, tmW;
-    if ((st = encode_operand(&tmX, xq, M_total, K, K, mpq::decode_x_box_rows())) != MPQ_OK)
-        return st;
-    if ((st = encode_operand(&tmW, B, G * N, K, ldb, 128)) != MPQ_OK)
-        return st;
-    mpq::FuseArgs f{};
-    f.x = reinterpret_cast<const uint16_t *>(A);
-    f.ldx = lda;
-    f.xq = xq; f.sx = sx; f.ready = ready;
-    f.pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
-    return from_cuda(mpq::launch_decode(tmX, tmW, a, out_dtype == MPQ_OUT_FP32, &f, h->num_sms,
-                                        static_cast<cudaStream_t>(stream)));
+    return launch_fused_grouped(h, h->workspace, G, d_offsets, M_total, N, K, A, lda, B, ldb, sB, ldsb, C, ldc,
+                                out_dtype, flags, stream);
 }
 
 // The allocation-free form of the fused grouped GEMM: the same validation and launch as
@@ -466,30 +489,8 @@ mpq_status fp8_grouped_gemm_fused_quant_noalloc(mpq_handle h, int64_t G, const i
     void *scratch = nullptr;
     if (mpq::noalloc_scratch(&scratch) != cudaSuccess)
         return MPQ_ERR_CUDA;
-    uint8_t *xq = static_cast<uint8_t *>(scratch);
-    float *sx = reinterpret_cast<float *>(xq + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
-    int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
-                                         align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
-                                                  sizeof(float)));
-    mpq::GemmArgs a{};
-    a.M = M_total; a.N = N; a.K = K;
-    a.sA = sx; a.ldsa = M_total;
-    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
-    a.C = C; a.ldc = ldc;
-    a.offsets = d_offsets; a.G = static_cast<int>(G);
-    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    CUtensorMap tmX, tmW;
-    if ((st = encode_operand(&tmX, xq, M_total, K, K, mpq::decode_x_box_rows())) != MPQ_OK)
-        return st;
-    if ((st = encode_operand(&tmW, B, G * N, K, ldb, 128)) != MPQ_OK)
-        return st;
-    mpq::FuseArgs f{};
-    f.x = static_cast<const uint16_t *>(X);
-    f.ldx = ldx;
-    f.xq = xq; f.sx = sx; f.ready = ready;
-    f.pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
-    return from_cuda(mpq::launch_decode(tmX, tmW, a, out_dtype == MPQ_OUT_FP32, &f, h->num_sms,
-                                        static_cast<cudaStream_t>(stream)));
+    return launch_fused_grouped(h, scratch, G, d_offsets, M_total, N, K, X, ldx, B, ldb, sB, ldsb, C, ldc, out_dtype,
+                                flags, stream);
 }
 
 mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
@@ -516,8 +517,9 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
         return MPQ_ERR_ALIGN;
     if (M_total == 0)
         return MPQ_OK;
-    const bool weight_tiles =
-        (flags & MPQ_GROUPED_WEIGHT_TILES) != 0 || ((flags & MPQ_GROUPED_ROW_TILES) == 0 && M_total <= 64 * G);
+    // Row tiles by default: on single-SM tiles they stream the weights at the HBM rate even
+    // for a few tokens per expert; weight tiles only on request.
+    const bool weight_tiles = (flags & MPQ_GROUPED_WEIGHT_TILES) != 0;
     mpq::GemmArgs a{};
     a.M = M_total; a.N = N; a.K = K;
     a.sA = sA; a.ldsa = ldsa;

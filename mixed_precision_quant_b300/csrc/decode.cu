@@ -88,29 +88,6 @@ struct Item {
     int nb;         // 128-row block of the expert's weight
 };
 
-// Wait until *count >= target (acquire at GPU scope), bounded like the mbarrier waits.
-__device__ __forceinline__ bool wait_count(const int *count, int target, const WaitCtl &c, int tag)
-{
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
-        if (v >= target)
-            return true;
-        if (*c.abort)
-            return false;
-        if (globaltimer_ns() - t0 > c.timeout_ns) {
-            *c.abort = 1;
-            if (c.status != nullptr && atomicCAS(c.status, 0, kStatusTimeout) == 0)
-                atomicExch(c.status + 1, tag);
-            return false;
-        }
-        __nanosleep(128);
-    }
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
     const uint64_t t0 = globaltimer_ns();
@@ -222,49 +199,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
     const uint32_t tmem_base = misc[0];
     const int T = gitem[G];
 
-    if (FUSE) {
-        // ------------------------------------------------------------ phase 1: quantize
-        // Blocks of 32 token rows over [goff[0], goff[G]); thread -> (row, 128-column group),
-        // consecutive threads on consecutive groups of a row (256 contiguous bytes each).
-        const int r_begin = goff[0], r_end = goff[G];
-        const int nblk = (r_end - r_begin + 31) / 32;
-        for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
-            const int r0 = r_begin + b * 32, r1 = r0 + 32 < r_end ? r0 + 32 : r_end;
-            const int ngroups = (r1 - r0) * KB;
-            for (int gi = threadIdx.x; gi < ngroups; gi += blockDim.x) {
-                const int r = r0 + gi / KB, kb = gi - (gi / KB) * KB;
-                const uint4 *src = reinterpret_cast<const uint4 *>(f.x + static_cast<int64_t>(r) * f.ldx + kb * DK);
-                uint32_t w[64];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const uint4 v = __ldg(src + q);
-                    w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-                }
-                uint4 out[8];
-                const float sc = quantize_group128(w, f.pow2 != 0, out);
-                uint4 *dst = reinterpret_cast<uint4 *>(f.xq + static_cast<int64_t>(r) * p.K + kb * DK);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = out[q];
-                f.sx[static_cast<int64_t>(kb) * M + r] = sc;
-            }
-            fence_proxy_async_global();   // the codes are read by TMA (async proxy)
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int lo = 0, hi = G - 1;   // first expert whose rows end after r0
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (goff[mid + 1] > r0) hi = mid; else lo = mid + 1;
-                }
-                for (int g = lo; g < G && goff[g] < r1; ++g) {
-                    const int a = goff[g] > r0 ? goff[g] : r0, e = goff[g + 1] < r1 ? goff[g + 1] : r1;
-                    if (e > a)
-                        atomicAdd(f.ready + g, e - a);
-                }
-            }
-        }
-    }
+    if (FUSE)
+        quantize_rows_phase(goff, G, M, KB, p.K, f);   // phase 1
 
     // Item t: expert g (last with gitem[g] <= t), then weight block fastest so that
     // neighbouring CTAs share the expert's tokens in L2 while streaming different weights.

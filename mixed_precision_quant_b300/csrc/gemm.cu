@@ -37,6 +37,7 @@
 // its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
+#include "quant_device.cuh"
 
 namespace mpq {
 namespace {
@@ -82,6 +83,7 @@ size_t smem_bytes(bool grouped) { return 1024 + Cfg<PAIR>::SMEM_MAIN + (grouped 
 
 // Sizes are validated on the host to stay below 2^31 rows / columns.
 struct Tile {
+    int g;            // expert (grouped), else 0
     int row0;         // first row of A / C handled by this CTA
     int row_end;      // one past the last valid row for this CTA
     int brow0;        // first row of B loaded by this CTA (TMA view [G*N, K] when grouped)
@@ -117,10 +119,10 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
     }
 }
 
-template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR>
+template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmArgs p)
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs p, const FuseArgs f)
 {
     using C = Cfg<PAIR>;
     constexpr int STAGES = C::STAGES;
@@ -234,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
 
+    if (FUSE)   // fused activation quantization: phase 1, all warps, before the roles split
+        quantize_rows_phase(goff, p.G, M, KB, p.K, f);
+
     const int MT = static_cast<int>((M + C::TILE_M - 1) / C::TILE_M);
     const int T = GROUPED ? gtile[p.G] : MT * NT;
 
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mt = t % MT, nt = t / MT;
             row0 = mt * C::TILE_M;
             rend = static_cast<int>(M);
+            ti.g = 0;
             ti.n0 = nt * BN;
             ti.brow0 = ti.n0;
             ti.sb_base = 0;
@@ -254,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (gtile[mid] <= t) lo = mid; else hi = mid - 1;
             }
             const int g = lo;
+            ti.g = g;
             const int local = t - gtile[g];
             const int mtg = static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
             const int nt = local / mtg, mt = local - nt * mtg;
@@ -278,6 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             for (int t = unit; t < T; t += nunits) {
                 const Tile ti = tile_of(t);
+                if (FUSE) {   // the expert's token codes are complete (phase 1 of all CTAs)
+                    if (!wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0180))
+                        goto producer_done;
+                    fence_proxy_async_global();
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(bar(C::BAR_DONE + s), ph ^ 1, ctl, 0x0100 | s))
@@ -356,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             for (int t = unit; t < T; t += nunits) {
                 const Tile ti = tile_of(t);
+                if (FUSE && !wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0380))
+                    goto scale_done;
                 const float *sbg = p.sB + ti.sb_base;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t j = it % SSLOTS, ph = (it / SSLOTS) & 1;
@@ -558,11 +572,11 @@ __global__ void wait_selftest_kernel(int *status, uint64_t timeout_ns)
     }
 }
 
-template <int SB, bool F32, bool GR, bool PAIR>
+template <int SB, bool F32, bool GR, bool PAIR, bool FUSE>
 cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
-                       int grid, cudaStream_t st)
+                       const FuseArgs &f, int grid, cudaStream_t st)
 {
-    auto kern = gemm_kernel<SB, F32, GR, PAIR>;
+    auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE>;
     const size_t smem = smem_bytes<PAIR>(GR);
     static bool configured = false;  // one attribute call per instantiation and process
     if (!configured) {
@@ -572,8 +586,8 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
             return e;
         configured = true;
     }
-    if (!PAIR) {
-        kern<<<grid, kThreads, smem, st>>>(tmA, tmB, tmC, a);
+    if (!PAIR && !FUSE) {
+        kern<<<grid, kThreads, smem, st>>>(tmA, tmB, tmC, a, f);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg{};
@@ -582,13 +596,20 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+    } else {
+        // Fused quantization: phase 2 waits on phase-1 work of every CTA, so all CTAs must be
+        // resident at once -- a cooperative launch guarantees it (or fails).
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a, f);
 }
 
 } // namespace
@@ -596,7 +617,7 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
 int gemm_b_box_rows(bool pair) { return pair ? Cfg<true>::B_ROWS : Cfg<false>::B_ROWS; }
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
-                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st)
+                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st, const FuseArgs *fuse)
 {
     const bool grouped = a.offsets != nullptr;
     if (grouped && a.G > kMaxGroups)
@@ -616,9 +637,19 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     } else {
         grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     }
+    const FuseArgs none{};
+    if (fuse != nullptr) {   // grouped, single-SM tiles, weight block scales; one CTA per SM
+        if (!grouped || pair || scale_b != kScaleBlockNK)
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaMemsetAsync(fuse->ready, 0, sizeof(int) * static_cast<size_t>(a.G), st);
+        if (e != cudaSuccess)
+            return e;
+        return out_fp32 ? launch_one<kScaleBlockNK, true, true, false, true>(tmA, tmB, tmC, a, *fuse, num_sms, st)
+                        : launch_one<kScaleBlockNK, false, true, false, true>(tmA, tmB, tmC, a, *fuse, num_sms, st);
+    }
 #define MPQ_G(SB, F32, GR, PR)                                                             \
     if (scale_b == SB && out_fp32 == F32 && grouped == GR && pair == PR)                   \
-        return launch_one<SB, F32, GR, PR>(tmA, tmB, tmC, a, grid, st);
+        return launch_one<SB, F32, GR, PR, false>(tmA, tmB, tmC, a, none, grid, st);
 #define MPQ_G2(SB, F32, GR) MPQ_G(SB, F32, GR, true) MPQ_G(SB, F32, GR, false)
     MPQ_G2(kScaleBlockNK, false, false)
     MPQ_G2(kScaleBlockNK, true, false)

@@ -49,21 +49,6 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
-// Block-scaled FP8 GEMM on tcgen05: C[M,N] = sum over 128-wide K slices of
-// (A_slice B_slice^T) * sA * sB, promoted into FP32 after every slice.
-// tmA covers A [rows, K] E4M3, tmB covers B [rows, K] E4M3 (both K-major, 128B swizzle).
-// `pair`: 2-CTA clusters sharing B through multicast; each CTA then loads B in boxes of
-// gemm_b_box_rows(true) = 128 rows, else 256.
-// tmC: output view [rows, N] (BF16 or FP32) with box 64 bytes x 32 rows, 64-byte swizzle.
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
-                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st);
-int gemm_b_box_rows(bool pair);
-
-// Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
-// Grouped GEMM for few tokens per expert (weights as the MMA's M operand, tokens as N):
-// tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
-// weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
-// the grouped launch_gemm (sB block scales [G][N/128][ldsb]); C is written directly.
 // Fused activation quantization: the token rows come as BF16 x [M, K] (ldx elements) and
 // are quantized 1x128 into the workspace (xq [M, K] codes, sx [K/128][M] scales, ready[G]
 // counts, cleared by the launcher) inside the same launch; tmX must then cover xq and
@@ -76,6 +61,25 @@ struct FuseArgs {
     int *ready;
     int pow2;
 };
+
+// Block-scaled FP8 GEMM on tcgen05: C[M,N] = sum over 128-wide K slices of
+// (A_slice B_slice^T) * sA * sB, promoted into FP32 after every slice.
+// tmA covers A [rows, K] E4M3, tmB covers B [rows, K] E4M3 (both K-major, 128B swizzle).
+// `pair`: 2-CTA clusters sharing B through multicast; each CTA then loads B in boxes of
+// gemm_b_box_rows(true) = 128 rows, else 256.
+// tmC: output view [rows, N] (BF16 or FP32) with box 64 bytes x 32 rows, 64-byte swizzle.
+// fuse != null: grouped GEMM with fused 1x128 activation quantization (single-SM tiles,
+// weight block scales): tmA must cover fuse->xq, a.sA / a.ldsa must be fuse->sx / M.
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
+                        int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st,
+                        const FuseArgs *fuse = nullptr);
+int gemm_b_box_rows(bool pair);
+
+// Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
+// Grouped GEMM for few tokens per expert (weights as the MMA's M operand, tokens as N):
+// tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
+// weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
+// the grouped launch_gemm (sB block scales [G][N/128][ldsb]); C is written directly.
 // Size of the fixed scratch area of fp8_grouped_gemm_fused_quant_noalloc (MPQ_NOALLOC_SCRATCH_BYTES),
 // and its device address on the current device (looked up on first use, then cached).
 constexpr size_t kNoallocScratchBytes = size_t(64) << 20;

@@ -7,6 +7,7 @@
 // quotient x / s.
 #pragma once
 #include "mpq_device.cuh"
+#include "mpq_internal.h"
 
 namespace mpq {
 
@@ -70,6 +71,79 @@ __device__ __forceinline__ float quantize_group128(const uint32_t (&w)[64], bool
     for (int q = 0; q < 8; ++q)
         out[q] = codes16(&w[q * 8], g);
     return g.s;
+}
+
+
+// Wait until *count >= target (acquire at GPU scope), bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count(const int *count, int target, const WaitCtl &c, int tag)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+        if (v >= target)
+            return true;
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            if (c.status != nullptr && atomicCAS(c.status, 0, kStatusTimeout) == 0)
+                atomicExch(c.status + 1, tag);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Phase 1 of the grouped GEMMs with fused activation quantization (all threads of the CTA
+// call it): the BF16 rows [goff[0], goff[G]) are quantized 1x128 -- the arithmetic of the
+// standalone quantizer -- into f.xq [M, K] and f.sx [K/128][M], in blocks of 32 rows striped
+// over the CTAs; each finished block is published by a fence and an atomic add to the
+// ready count of every expert it overlaps.  Thread -> (row, 128-column group), consecutive
+// threads on consecutive groups of a row (256 contiguous bytes each).
+__device__ __forceinline__ void quantize_rows_phase(const int *goff, int G, int64_t M, int KB, int64_t K,
+                                                    const FuseArgs &f)
+{
+    const int r_begin = goff[0], r_end = goff[G];
+    const int nblk = (r_end - r_begin + 31) / 32;
+    for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
+        const int r0 = r_begin + b * 32, r1 = r0 + 32 < r_end ? r0 + 32 : r_end;
+        const int ngroups = (r1 - r0) * KB;
+        for (int gi = threadIdx.x; gi < ngroups; gi += blockDim.x) {
+            const int r = r0 + gi / KB, kb = gi - (gi / KB) * KB;
+            const uint4 *src = reinterpret_cast<const uint4 *>(f.x + static_cast<int64_t>(r) * f.ldx + kb * 128);
+            uint32_t w[64];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const uint4 v = __ldg(src + q);
+                w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+            }
+            uint4 out[8];
+            const float sc = quantize_group128(w, f.pow2 != 0, out);
+            uint4 *dst = reinterpret_cast<uint4 *>(f.xq + static_cast<int64_t>(r) * K + kb * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[q] = out[q];
+            f.sx[static_cast<int64_t>(kb) * M + r] = sc;
+        }
+        fence_proxy_async_global();   // the codes are read by TMA (async proxy)
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int lo = 0, hi = G - 1;   // first expert whose rows end after r0
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (goff[mid + 1] > r0) hi = mid; else lo = mid + 1;
+            }
+            for (int g = lo; g < G && goff[g] < r1; ++g) {
+                const int a = goff[g] > r0 ? goff[g] : r0, e = goff[g + 1] < r1 ? goff[g + 1] : r1;
+                if (e > a)
+                    atomicAdd(f.ready + g, e - a);
+            }
+        }
+    }
 }
 
 } // namespace mpq

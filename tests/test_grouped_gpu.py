@@ -148,8 +148,9 @@ def test_moe_decode_full_size_sampled(mpq, tiles):
     ([256, 17, 64], 0, 9),
 ])
 def test_fused_quant_equals_two_steps(mpq, counts, lead, trail, pow2):
-    """One fused launch == 1x128 quantizer then the weight-tile GEMM, bit for bit, and the
-    workspace holds exactly the standalone quantizer's codes and scales."""
+    """One fused launch == 1x128 quantizer then the same grouped GEMM (row tiles, and weight
+    tiles on request), bit for bit, and the workspace holds exactly the standalone
+    quantizer's codes and scales."""
     G, N, K = len(counts), 256, 384
     off = np.concatenate([[0], np.cumsum(counts)]) + lead
     M = int(off[-1]) + trail
@@ -159,13 +160,15 @@ def test_fused_quant_equals_two_steps(mpq, counts, lead, trail, pow2):
     offs = _dev(off.astype(np.int64))
     qbd, sbd = _dev(qb), _dev(sb)
     qx, sx, _, _ = mpq.fp8_quant_tile_1x128(x, pow2=pow2)
-    C2 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
-    mpq.fp8_grouped_gemm_blockscaled(offs, qx, sx, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C2, tiles="weights")
-    C1 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
-    mpq.fp8_grouped_gemm_blockscaled(offs, x, None, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C1, fuse_quant=True,
-                                     pow2=pow2)
-    torch.cuda.synchronize()
-    assert torch.equal(C1, C2)
+    for tiles in ("auto", "weights"):   # fused on row tiles (default) and on weight tiles
+        C2 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
+        mpq.fp8_grouped_gemm_blockscaled(offs, qx, sx, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C2,
+                                         tiles="rows" if tiles == "auto" else tiles)
+        C1 = torch.full((M, N), 777.0, dtype=torch.float32, device="cuda")
+        mpq.fp8_grouped_gemm_blockscaled(offs, x, None, qbd, sbd, out_dtype=mpq.OUT_FP32, C=C1, fuse_quant=True,
+                                         pow2=pow2, tiles=tiles)
+        torch.cuda.synchronize()
+        assert torch.equal(C1, C2), tiles
     ws = mpq._workspaces[torch.cuda.current_device()]
     r0, r1 = int(off[0]), int(off[-1])
     codes = ws[:M * K].view(M, K)
