@@ -434,7 +434,7 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak):
                                                                      pow2=pow2), flush)
                 res[proj]["fused"] = {"ms": round(fms, 4), "weight_GBps": round(gb(wb, fms), 1),
                                       "frac_hbm_weights": round(gb(wb, fms) / hbm, 4),
-                                      "path": "one launch: fused 1x128 quantization + weight-tile grouped GEMM"}
+                                      "path": "one cooperative launch: 1x128 quantization phase + row-tile grouped GEMM"}
                 fused_ms += fms
             total_ms += ms
             total_flops += fl
