@@ -67,6 +67,8 @@ def _load():
         lib.mpqo_quant_tile_128x1.argtypes = [P, I, I, I, P, I, P, I, ctypes.c_int]
         lib.mpqo_quant_block_128x128.restype = None
         lib.mpqo_quant_block_128x128.argtypes = [P, I, I, I, P, I, P, I, P, I, ctypes.c_int]
+        lib.mpqo_requant_tile_128x1.restype = None
+        lib.mpqo_requant_tile_128x1.argtypes = [P, I, I, I, P, I, P, I, P, I, ctypes.c_int]
         lib.mpqo_gemm_ref.restype = None
         lib.mpqo_gemm_ref.argtypes = [ctypes.c_int, I, I, I, P, I, P, I, P, I, P, I, P, P, I]
         lib.mpqo_gemm_ref_at.restype = None
@@ -144,6 +146,22 @@ def quant_tile_128x1(x_bf16_bits: np.ndarray, pow2: bool = False):
     qT = np.empty((cols, rows), np.uint8)
     sT = np.empty((rows // 128, cols), np.float32)
     _load().mpqo_quant_tile_128x1(_ptr(x), rows, cols, cols, _ptr(qT), rows, _ptr(sT), cols, int(pow2))
+    return qT, sT
+
+
+def requant_tile_128x1(q: np.ndarray, s: np.ndarray, pow2: bool = False):
+    """Re-quantize a row-wise 1x128 quantization (codes q uint8 [rows, cols], scales s
+    float32 [cols/128, rows]) into 128x1 groups along rows: dequantize to binary32
+    (dec(q) * s), then quantize the column groups.  Returns (qT uint8 [cols, rows],
+    sT float32 [rows/128, cols])."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    rows, cols = q.shape
+    assert rows % 128 == 0 and cols % 128 == 0 and s.shape == (cols // 128, rows)
+    qT = np.empty((cols, rows), np.uint8)
+    sT = np.empty((rows // 128, cols), np.float32)
+    _load().mpqo_requant_tile_128x1(_ptr(q), rows, cols, cols, _ptr(s), rows, _ptr(qT), rows, _ptr(sT), cols,
+                                    int(pow2))
     return qT, sT
 
 

@@ -34,7 +34,9 @@
  *   - an all-zero group gets scale 1.0;
  *   - power-of-2 scales round up: s = 2^e with e the smallest integer such that
  *     amax <= 448 * 2^e, so no element saturates;
- *   - zero keeps its sign (-0 -> 0x80), NaN inputs are out of contract.
+ *   - zero keeps its sign (-0 -> 0x80), NaN inputs are out of contract;
+ *   - a positive scale never drops below 2^-149 (see mpqo_group_scale);
+ *   - re-quantization dequantizes with one binary32 product dec(q) * s.
  *
  * Build: gcc -O2 -fPIC -shared -ffp-contract=off (no -ffast-math: IEEE division,
  * subnormals kept).
@@ -117,17 +119,23 @@ static float bf16_to_float(uint16_t b)
     return x.f;
 }
 
-/* Scale of one quantization group from its maximum absolute value. */
+/* Scale of one quantization group from its maximum absolute value.
+ * Floor: a scale that would be 0 (amax/448 below half the smallest subnormal) or a power
+ * of 2 below 2^-149 (not a binary32 number) becomes 2^-149, the smallest positive
+ * binary32.  BF16 groups never reach it (their amax is at least 2^-133); groups of
+ * dequantized FP8 values can. */
 float mpqo_group_scale(float amax, int pow2)
 {
     if (amax == 0.0f)
         return 1.0f;
-    if (!pow2)
-        return amax / 448.0f; /* one IEEE binary32 division */
-    int e = -160;
+    if (!pow2) {
+        float s = amax / 448.0f; /* one IEEE binary32 division */
+        return s > 0.0f ? s : ldexpf(1.0f, -149);
+    }
+    int e = -149;
     while ((double)amax > ldexp(448.0, e))
         ++e;
-    return ldexpf(1.0f, e); /* 2^e, e >= -141 for any BF16 amax */
+    return ldexpf(1.0f, e); /* 2^e */
 }
 
 static uint8_t quant_one(float x, float s)
@@ -181,6 +189,40 @@ void mpqo_quant_tile_128x1(const uint16_t *x, int64_t rows, int64_t cols, int64_
             for (int i = 0; i < 128; ++i)
                 qT[c * ldqT + rb * 128 + i] =
                     quant_one(bf16_to_float(x[(rb * 128 + i) * ldx + c]), sc);
+        }
+    }
+}
+
+/* Re-quantization of cached FP8 codes into 128x1 groups.  Page 2 ("9 Amazing Deepseek
+ * Hacks"), last paragraph: in the backward pass the FP8 matrix is read out, dequantized,
+ * transposed and quantized again into 128x1 tiles; page 1, second paragraph: activations
+ * are cached in FP8 for the backward pass of the Linear operator.
+ * Input: the row-wise 1x128 quantization of a [rows, cols] matrix, codes q[t, c] (ldq) and
+ * scales s[(c/128) * lds + t].  Each element is dequantized to binary32,
+ * xhat = dec(q) * s (one IEEE binary32 product), and the 128x1 groups of xhat along t are
+ * quantized as mpqo_quant_tile_128x1 quantizes BF16 values.  Output stored transposed:
+ * qT[c, t] (ldqT), sT[(t/128) * ldsT + c]. */
+void mpqo_requant_tile_128x1(const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq,
+                             const float *s, int64_t lds, uint8_t *qT, int64_t ldqT,
+                             float *sT, int64_t ldsT, int pow2)
+{
+    int64_t nrb = rows / 128;
+    for (int64_t c = 0; c < cols; ++c) {
+        for (int64_t rb = 0; rb < nrb; ++rb) {
+            float xh[128];
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                int64_t t = rb * 128 + i;
+                float d = (float)mpqo_e4m3_decode(q[t * ldq + c]); /* exact */
+                xh[i] = d * s[(c / 128) * lds + t];
+                float a = fabsf(xh[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            float sc = mpqo_group_scale(amax, pow2);
+            sT[rb * ldsT + c] = sc;
+            for (int i = 0; i < 128; ++i)
+                qT[c * ldqT + rb * 128 + i] = quant_one(xh[i], sc);
         }
     }
 }

@@ -375,3 +375,78 @@ def test_grouped_matches_per_expert_dense():
     for g in range(G):
         expect[off[g]:off[g + 1]] = Ad[off[g]:off[g + 1]] @ Bd[g].T
     assert np.array_equal(ref, expect)
+
+
+# ------------------------------------------- re-quantization of cached FP8 into 128x1
+
+def test_scale_floor():
+    """A positive max-abs never gives a zero scale: below 448 * 2^-149 (power of 2) or
+    224 * 2^-149 (amax / 448 rounding to 0) the scale is 2^-149, the smallest positive
+    binary32; just above, the ordinary rule applies."""
+    tiny = np.float32(2.0 ** -149)
+    for pow2 in (False, True):
+        assert oracle.group_scale(tiny, pow2) == tiny
+        assert oracle.group_scale(np.float32(224 * 2.0 ** -149), pow2) == tiny
+        assert oracle.group_scale(np.float32(448 * 2.0 ** -149), pow2) == tiny
+    # 449 * 2^-149 needs 2^-148 as a power of 2; amax / 448 rounds to 2^-149
+    assert oracle.group_scale(np.float32(449 * 2.0 ** -149), True) == np.float32(2.0 ** -148)
+    assert oracle.group_scale(np.float32(449 * 2.0 ** -149), False) == tiny
+    # BF16's smallest subnormal is far above the floor
+    assert oracle.group_scale(np.float32(2.0 ** -133), True) == np.float32(2.0 ** -141)
+
+
+def _requant_constructed(rows, cols, rng):
+    """Choose the re-quantization's answer first: output codes Qo [rows, cols] with
+    magnitudes in [4, 64] plus one +-448 per 128x1 column group, and power-of-2 output
+    scales So[rows/128, cols] in 2^-6 .. 1, so xhat = dec(Qo) So is exact.  Then factor
+    xhat into a 1x128 input: scales s[cols/128, rows] = 2^k (k = 0, 1, 2) and codes
+    q = encode(xhat / s), exact because xhat / s stays in the E4M3 normal range."""
+    mags = rng.integers(0x48, 0x70, size=(rows, cols)).astype(np.uint8)   # 4 .. 60
+    signs = (rng.integers(0, 2, size=(rows, cols)) * 0x80).astype(np.uint8)
+    qo = mags | signs
+    for rb in range(rows // 128):
+        for c in range(cols):
+            t = rb * 128 + rng.integers(128)
+            qo[t, c] = 0x7E | (qo[t, c] & 0x80)
+    so = (2.0 ** rng.integers(-6, 1, size=(rows // 128, cols))).astype(np.float32)
+    xhat = torch_decode(qo) * np.repeat(so, 128, axis=0)
+    s_in = (2.0 ** rng.integers(0, 3, size=(cols // 128, rows))).astype(np.float32)
+    s_full = np.repeat(s_in.T, 128, axis=1)                                # [rows, cols]
+    q = torch_encode((xhat / s_full).astype(np.float32))
+    assert np.array_equal(torch_decode(q) * s_full, xhat)                 # exact factorisation
+    return q, s_in, qo, so
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_requant_by_construction(pow2):
+    rng = np.random.default_rng(31)
+    q, s, qo, so = _requant_constructed(256, 384, rng)
+    qT, sT = oracle.requant_tile_128x1(q, s, pow2=pow2)
+    assert np.array_equal(qT, qo.T)
+    assert np.array_equal(sT, so)
+
+
+def test_requant_equals_128x1_quantizer_of_dequantized_values():
+    """With power-of-2 input scales, dec(q) * s is exact and fits BF16 (four significant
+    bits), so re-quantizing equals the 128x1 quantizer applied to the dequantized matrix."""
+    rng = np.random.default_rng(32)
+    x = (rng.standard_normal((384, 256)) * np.exp(rng.uniform(-6, 6, (384, 1)))
+         * rng.choice([1.0, 1.0, 40.0], size=(1, 256))).astype(np.float32)
+    q, s = oracle.quant_tile_1x128((x.view(np.uint32) >> 16).astype(np.uint16), pow2=True)
+    xhat = (torch_decode(q) * np.repeat(s.T, 128, axis=1)).astype(np.float32)
+    xb = bf16_bits(xhat)
+    assert np.array_equal(((xb.astype(np.uint32) << 16).view(np.float32)), xhat)
+    for pow2 in (False, True):
+        qT, sT = oracle.requant_tile_128x1(q, s, pow2=pow2)
+        q2, s2 = oracle.quant_tile_128x1(xb, pow2=pow2)
+        assert np.array_equal(qT, q2) and np.array_equal(sT, s2)
+
+
+def test_requant_zero_and_signed_zero_groups():
+    q = np.zeros((128, 256), np.uint8)
+    q[:, 128:] = 0x80                                      # -0
+    s = np.full((2, 128), 3.0, np.float32)
+    qT, sT = oracle.requant_tile_128x1(q, s)
+    assert np.all(sT == 1.0)
+    assert np.all(qT[:128] == 0) and np.all(qT[128:] == 0x80)
+
