@@ -371,6 +371,13 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak):
     nbytes = T * Kin * (2 + 2 + 8 / 128)
     out["dual_quant_X_8192x7168"] = {"ms": round(ms, 4), "GBps": round(gb(nbytes, ms), 1),
                                      "frac_hbm": round(gb(nbytes, ms) / hbm, 4), "bound": "hbm"}
+    # re-quantization of the cached FP8 X (codes + 1x128 scales) into 128x1 groups
+    rqT, rsT = mpq.fp8_requant_tile_128x1(qx, sx)
+    ms = timed(lambda: mpq.fp8_requant_tile_128x1(qx, sx, qT=rqT, sT=rsT), flush)
+    nbytes = T * Kin * (1 + 1 + 8 / 128)
+    out["requant_X_8192x7168"] = {"ms": round(ms, 4), "GBps": round(gb(nbytes, ms), 1),
+                                  "frac_hbm": round(gb(nbytes, ms) / hbm, 4), "bound": "hbm"}
+    del rqT, rsT
     qdy, sdy, qdyT, sdyT = mpq.fp8_quant_tile_1x128(dY, pow2=True, transposed=True)
     ms = timed(lambda: mpq.fp8_quant_tile_1x128(dY, pow2=True, q=qdy, s=sdy, qT=qdyT, sT=sdyT, transposed=True), flush)
     nbytes = T * Nout * (2 + 2 + 8 / 128)

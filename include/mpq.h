@@ -154,6 +154,34 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
                                 uint32_t flags, void *stream);
 
 /*
+ * fp8_requant_tile_128x1 -- re-quantization of a cached FP8 activation into 128x1 groups
+ * (page 2, last paragraph: in the backward pass the FP8 matrix is read out, dequantized,
+ * transposed and re-quantized into 128x1 tiles; page 1, second paragraph: activations are
+ * cached in FP8 for the backward pass).  The input is what fp8_quant_tile_1x128 writes;
+ * the output has the layout of its transposed part, so it feeds the Wgrad GEMM directly.
+ *
+ *   q  [rows, cols] E4M3, ldq >= cols (device, read only);
+ *   s  [cols/128][lds] float32, lds >= rows: s[kb*lds + r] scales q[r, kb*128 .. +127];
+ *   qT [cols, rows] E4M3, ldqT >= rows (device, written);
+ *   sT [rows/128][ldsT] float32, ldsT >= cols (device, written).
+ *   flags: 0 or MPQ_POW2 (the scale rule of the output groups).
+ * Each element is dequantized to binary32 as dec(q) * s (one rounded product); the values
+ * x[rb*128 .. rb*128+127, c] form one group, quantized as fp8_quant_tile_1x128 quantizes
+ * its groups: qT[c, r] is the code of x[r, c], sT[rb*ldsT + c] the group's scale.  A
+ * positive max-abs value never gives a scale below 2^-149 (the smallest positive
+ * binary32): a smaller power of 2, or a quotient amax/448 that rounds to 0, is raised to
+ * it (BF16 inputs never reach this; dequantized FP8 values can).  The dequantized values
+ * must be finite, as they are for any codes and scales fp8_quant_tile_1x128 writes.
+ * Requirements: rows % 128 == 0, cols % 128 == 0, rows >= 0; q, qT, s 16-byte aligned;
+ * ldq, ldqT % 16 == 0; lds % 4 == 0; sT 4-byte aligned (pointers and alignment are not
+ * checked when rows == 0: then nothing is read or written).  The input and output must not overlap.  Asynchronous on
+ * `stream`; nothing is allocated.
+ */
+mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq,
+                                  const float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sT,
+                                  int64_t ldsT, uint32_t flags, void *stream);
+
+/*
  * fp8_quant_block_128x128 -- weight quantization in 128x128 blocks (page 1, second
  * paragraph: weights are quantized online from their max-abs value), optionally also
  * writing the transposed codes (same scales) used as the Dgrad B operand.

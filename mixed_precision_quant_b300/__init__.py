@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "mpq_check_device_status": (INT, [P, P, ctypes.POINTER(INT)]),
         "fp8_quant_tile_1x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, P, I, U32, P]),
         "fp8_quant_block_128x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
+        "fp8_requant_tile_128x1": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
         "fp8_gemm_blockscaled": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
         "fp8_grouped_gemm_blockscaled": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, U32, P]),
         "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
@@ -147,6 +148,25 @@ def fp8_quant_tile_1x128(x: torch.Tensor, *, pow2: bool = False, rows_out: bool 
                                    _stream(dev, stream))
     _check("fp8_quant_tile_1x128", st)
     return q, s, qT, sT
+
+
+def fp8_requant_tile_128x1(q: torch.Tensor, s: torch.Tensor, *, pow2: bool = False, qT=None, sT=None,
+                           stream=None):
+    """Re-quantize a cached 1x128 quantization (codes ``q [rows, cols]`` uint8, scales
+    ``s [cols/128, rows]`` float32, as written by :func:`fp8_quant_tile_1x128`) into 128x1
+    groups along rows: each value is dequantized to binary32 (``dec(q) * s``) and the
+    column groups are quantized again.  Returns ``(qT [cols, rows], sT [rows/128, cols])``,
+    the layout of the transposed quantizer output."""
+    _cuda2d(q, torch.uint8, "q")
+    _cuda2d(s, torch.float32, "s")
+    rows, cols = q.shape
+    dev = q.device
+    qT = qT if qT is not None else torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    sT = sT if sT is not None else torch.empty((rows // 128, cols), dtype=torch.float32, device=dev)
+    st = _lib.fp8_requant_tile_128x1(_handle(dev), _ptr(q), rows, cols, _ld(q), _ptr(s), _ld(s), _ptr(qT), _ld(qT),
+                                     _ptr(sT), _ld(sT), POW2 if pow2 else 0, _stream(dev, stream))
+    _check("fp8_requant_tile_128x1", st)
+    return qT, sT
 
 
 def fp8_quant_block_128x128(w: torch.Tensor, *, pow2: bool = False, transposed: bool = False,

@@ -282,6 +282,40 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
     return from_cuda(mpq::launch_quant_dual(tmx, tmq, tmqT, a, pow2, h->num_sms, st));
 }
 
+mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq,
+                                  const float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sT,
+                                  int64_t ldsT, uint32_t flags, void *stream)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if (flags & ~MPQ_POW2)
+        return MPQ_ERR_UNSUPPORTED;
+    if (rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0 || ldq < cols || lds < rows ||
+        ldqT < rows || ldsT < cols)
+        return MPQ_ERR_SHAPE;
+    if (rows == 0)   // nothing is read or written
+        return MPQ_OK;
+    if (q == nullptr || s == nullptr || qT == nullptr || sT == nullptr)
+        return MPQ_ERR_NULL;
+    if (!aligned(q, 16) || ldq % 16 != 0 || !aligned(s, 16) || lds % 4 != 0 || !aligned(qT, 16) ||
+        ldqT % 16 != 0 || !aligned(sT, 4))
+        return MPQ_ERR_ALIGN;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return MPQ_ERR_SHAPE;
+    mpq::RequantArgs a{};
+    a.rows = rows; a.cols = cols;
+    a.s = s; a.lds = lds; a.sT = sT; a.ldsT = ldsT;
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    CUtensorMap tmq, tmqT;
+    mpq_status e = encode_codes(&tmq, const_cast<uint8_t *>(q), rows, cols, ldq);
+    if (e == MPQ_OK)
+        e = encode_codes(&tmqT, qT, cols, rows, ldqT);
+    if (e != MPQ_OK)
+        return e;
+    return from_cuda(mpq::launch_requant(tmq, tmqT, a, (flags & MPQ_POW2) != 0, h->num_sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, int64_t cols, int64_t ldw,
                                    uint8_t *q, int64_t ldq, uint8_t *qT, int64_t ldqT, float *s, int64_t lds,
                                    uint32_t flags, void *stream)

@@ -102,6 +102,15 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Plain bulk copy global -> shared (both addresses 16-byte aligned, size a multiple of 16),
+// completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 2-D tiled bulk tensor load into shared memory, completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int32_t x, int32_t y)
@@ -366,6 +375,7 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 
 // Wait until at most the three most recent committed bulk stores of this thread still read
 // shared memory.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read3() { asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); }
 
 // Wait until every committed bulk store of this thread has completed.
@@ -463,8 +473,11 @@ __device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
         g.s = 1.0f; g.r = 1.0f; g.mode = 1;
         return g;
     }
+    // Floor: a positive max-abs never yields a zero scale; 2^-149, the smallest positive
+    // binary32, replaces a power of 2 below it or a quotient amax / 448 that rounds to 0.
+    // BF16 groups never reach it (max-abs >= 2^-133); dequantized FP8 values can.
     if (pow2) {
-        const int e = pow2_exponent(amax);
+        const int e = max(pow2_exponent(amax), -149);
         g.s = exp2_int(e);
         if (e >= -126) { g.r = exp2_int(-e); g.mode = 1; }
         else { g.r = 0.0f; g.mode = 2; }
@@ -472,6 +485,7 @@ __device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
     }
     g.s = __fdiv_rn(amax, 448.0f);
     if (g.s < kMinCorrectedScale) {
+        g.s = fmaxf(g.s, 0x1p-149f);
         g.r = 0.0f; g.mode = 2;
         return g;
     }

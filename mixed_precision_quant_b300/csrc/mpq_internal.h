@@ -24,6 +24,20 @@ struct QuantArgs {
     uint64_t timeout_ns;
 };
 
+// Re-quantization of a cached 1x128 quantization into 128x1 groups (codes travel by TMA).
+struct RequantArgs {
+    int64_t rows, cols;   // of the input codes [rows, cols]; both multiples of 128
+    const float *s;       // input scales [cols/128][lds]
+    int64_t lds;
+    float *sT;            // output scales [rows/128][ldsT]
+    int64_t ldsT;
+    int *status;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_requant(const CUtensorMap &tmq, const CUtensorMap &tmqT, const RequantArgs &a, bool pow2,
+                           int num_sms, cudaStream_t st);
+
 cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
                               int num_sms, cudaStream_t st);
 cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,

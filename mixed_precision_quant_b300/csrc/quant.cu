@@ -22,6 +22,9 @@
 //   * codes are written into 128-byte-swizzled staging tiles, one per warpgroup, and
 //     leave with TMA bulk-tensor stores (coalesced, clipped at the tensor bounds).
 // Every wait is bounded.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
 #include "quant_device.cuh"
@@ -446,6 +449,144 @@ cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream
     return cudaGetLastError();
 }
 
+// ------------------------------------ re-quantization of cached FP8 into 128x1 groups
+//
+// Page 2 ("9 Amazing Deepseek Hacks"), last paragraph: in the backward pass the cached FP8
+// matrix is read out, dequantized, transposed and quantized again into 128x1 tiles.  Input:
+// codes q[t, c] of a 1x128 quantization with scales s[(c/128) lds + t]; each element is
+// dequantized to binary32 (dec(q) * s, one rounded product), and each column's 128 values
+// of a 128-row block form one group, written transposed: qT[c, t], sT[(t/128) ldsT + c].
+//
+// Tiles of 128 rows x 128 columns of codes (16 KB) and their 128 row scales stream through
+// a TMA ring.  Consumer thread (cp, qd) owns columns 2cp, 2cp+1 and rows 32qd .. +31 of the
+// tile: it reads code pairs with 2-byte shared loads (the two columns of one row,
+// conflict-free), keeps its 64 dequantized values in registers, and the four row quarters'
+// max-abs values meet in shared memory.  Each column's 32 codes go to the swizzled staging
+// tile as two 16-byte pieces of row c, which leaves with one TMA store per tile.  Two CTAs
+// share an SM, so one's tile latency (barriers, conversion) overlaps the other's.
+constexpr int RQ_STAGES = 4;
+constexpr int kRqCtasPerSm = 2;
+constexpr uint32_t kRqScales = 128 * 4;   // one tile's row scales
+constexpr size_t kRqSmem =
+    1024 + RQ_STAGES * kBox + 2 * kBox + RQ_STAGES * kRqScales + 4 * 128 * 4 + (2 * RQ_STAGES + 2) * 8 + 16;
+
+template <bool POW2>
+__global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
+    requant_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmqT,
+                   const RequantArgs p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base0 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
+    const uint32_t stage = base0 + pad, out = stage + RQ_STAGES * kBox, scl = out + 2 * kBox;
+    float *red = reinterpret_cast<float *>(smem_raw + pad + (RQ_STAGES + 2) * kBox + RQ_STAGES * kRqScales);
+    const uint32_t bars = smem_u32(red + 4 * 128);   // full[S], empty[S], syncA, syncB
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 4 * 128 + (2 * RQ_STAGES + 2) * 2);
+    const uint32_t full = bars, empty = bars + 8 * RQ_STAGES, syncA = bars + 16 * RQ_STAGES, syncB = syncA + 8;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RQ_STAGES; ++i) {
+            mbar_init(full + 8 * i, 1);
+            mbar_init(empty + 8 * i, kConsumers);
+        }
+        mbar_init(syncA, kConsumers);
+        mbar_init(syncB, kConsumers);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    if (warp == kConsumers) {   // producer: one 128 x 128 box of codes per tile
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+                const uint32_t st = it % RQ_STAGES, ph = (it / RQ_STAGES) & 1;
+                if (!mbar_wait(empty + 8 * st, ph ^ 1, ctl, 0x1800 | st))
+                    break;
+                const int64_t tb = item / ncb, cb = item - tb * ncb;
+                mbar_arrive_expect_tx(full + 8 * st, kBox + kRqScales);
+                tma_load_2d(stage + st * kBox, &tmq, full + 8 * st, static_cast<int32_t>(cb * 128),
+                            static_cast<int32_t>(tb * 128));
+                bulk_load(scl + st * kRqScales, p.s + cb * p.lds + tb * 128, kRqScales, full + 8 * st);
+            }
+            for (uint32_t j = it > RQ_STAGES ? it - RQ_STAGES : 0; j < it; ++j) {   // no load left in flight
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(full + 8 * (j % RQ_STAGES), (j / RQ_STAGES) & 1))
+                    if (globaltimer_ns() - t0 > p.timeout_ns)
+                        break;
+            }
+        }
+        return;
+    }
+    const int cp = lane + 32 * (warp & 1), qd = warp >> 1, c = 2 * cp;
+    const bool elected = threadIdx.x == 0;
+    uint32_t kA = 0, kB = 0, it = 0;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+        const int64_t tb = item / ncb, cb = item - tb * ncb;
+        const uint32_t st = it % RQ_STAGES, ph = (it / RQ_STAGES) & 1;
+        if (!mbar_wait(full + 8 * st, ph, ctl, 0x1810 | st))
+            break;
+        const uint32_t tile = stage + st * kBox;
+        float sc[32];   // input scales of rows 32qd .. +31 (the same for every lane: broadcast)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = lds_v4(scl + st * kRqScales + (32 * qd + 4 * j) * 4);
+            sc[4 * j] = __uint_as_float(v.x); sc[4 * j + 1] = __uint_as_float(v.y);
+            sc[4 * j + 2] = __uint_as_float(v.z); sc[4 * j + 3] = __uint_as_float(v.w);
+        }
+        float xa[32], xb[32], ma = 0.0f, mb = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int t = 32 * qd + i;
+            const uint32_t pair = lds_u16(tile + sw128(t, cp >> 3) + ((2 * cp) & 15));
+            const __half2 h(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3));
+            const float2 d = __half22float2(h);   // exact: every E4M3 value is an FP16 value
+            xa[i] = __fmul_rn(d.x, sc[i]);        // column c (the pair's low byte)
+            xb[i] = __fmul_rn(d.y, sc[i]);        // column c + 1
+            ma = fmaxf(ma, fabsf(xa[i]));
+            mb = fmaxf(mb, fabsf(xb[i]));
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty + 8 * st);
+        *reinterpret_cast<float2 *>(red + qd * 128 + c) = make_float2(ma, mb);
+        if (elected)
+            bulk_wait_read1();   // the store of two tiles ago has left this tile's staging buffer
+        if (!wg_sync(syncA, kA, ctl, 0x1820))
+            break;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 v = *reinterpret_cast<const float2 *>(red + q * 128 + c);
+            ma = fmaxf(ma, v.x);
+            mb = fmaxf(mb, v.y);
+        }
+        const GroupScale ga = make_group_scale(ma, POW2), gb = make_group_scale(mb, POW2);
+        uint32_t wa[8], wb[8];
+        codes_f32<32>(xa, ga, wa);
+        codes_f32<32>(xb, gb, wb);
+        const uint32_t stg = out + (it & 1) * kBox;
+        sts_v4(stg + sw128(c, 2 * qd), make_uint4(wa[0], wa[1], wa[2], wa[3]));
+        sts_v4(stg + sw128(c, 2 * qd + 1), make_uint4(wa[4], wa[5], wa[6], wa[7]));
+        sts_v4(stg + sw128(c + 1, 2 * qd), make_uint4(wb[0], wb[1], wb[2], wb[3]));
+        sts_v4(stg + sw128(c + 1, 2 * qd + 1), make_uint4(wb[4], wb[5], wb[6], wb[7]));
+        fence_proxy_async_smem();
+        if (qd == 0) {
+            float *dst = p.sT + tb * p.ldsT + cb * 128 + c;
+            dst[0] = ga.s;
+            dst[1] = gb.s;
+        }
+        if (!wg_sync(syncB, kB, ctl, 0x1821))
+            break;
+        if (elected) {
+            tma_store_2d(&tmqT, stg, static_cast<int32_t>(tb * 128), static_cast<int32_t>(cb * 128));
+            bulk_commit();
+        }
+    }
+    if (elected)
+        bulk_wait0();
+}
+
 } // namespace
 
 cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
@@ -492,6 +633,17 @@ cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, c
                   : launch_q(quant_block_kernel<true, false>, smem_n, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a);
     return tr ? launch_q(quant_block_kernel<false, true>, smem_t, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a)
               : launch_q(quant_block_kernel<false, false>, smem_n, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a);
+}
+
+cudaError_t launch_requant(const CUtensorMap &tmq, const CUtensorMap &tmqT, const RequantArgs &a, bool pow2,
+                           int num_sms, cudaStream_t st)
+{
+    const int64_t items = (a.rows / 128) * (a.cols / 128);
+    if (items == 0)
+        return cudaSuccess;
+    const int ctas = kRqCtasPerSm * num_sms;
+    return pow2 ? launch_q(requant_kernel<true>, kRqSmem, items, ctas, st, kQThreads, tmq, tmqT, a)
+                : launch_q(requant_kernel<false>, kRqSmem, items, ctas, st, kQThreads, tmq, tmqT, a);
 }
 
 } // namespace mpq

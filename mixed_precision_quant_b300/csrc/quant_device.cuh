@@ -64,6 +64,38 @@ __device__ __forceinline__ void codes_words(const uint32_t *w, const GroupScale 
         out[j] = (c[2 * j] | (c[2 * j + 1] << 16)) ^ flip;
 }
 
+// N binary32 values (consecutive in the output row) -> N E4M3 codes (N/4 words), the
+// same arithmetic as codes_words for values that are not BF16.
+template <int N>
+__device__ __forceinline__ void codes_f32(const float *x, const GroupScale &g, uint32_t *out)
+{
+    uint32_t c[N / 2];
+    uint32_t flip = 0;
+    if (g.mode == 0) {
+        const unsigned long long nr = pack2(-g.r, -g.r), s2 = pack2(g.s, g.s);
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+            const unsigned long long t = neg_quotient2(pack2(x[2 * j], x[2 * j + 1]), nr, s2);
+            c[j] = e4m3x2(lo_of(t), hi_of(t));
+        }
+        flip = 0x80808080u;
+    } else if (g.mode == 1) {
+        const unsigned long long r = pack2(g.r, g.r);
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+            const unsigned long long p = fmul2(pack2(x[2 * j], x[2 * j + 1]), r);
+            c[j] = e4m3x2(lo_of(p), hi_of(p));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j)
+            c[j] = e4m3_pair(x[2 * j], x[2 * j + 1], g);
+    }
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j)
+        out[j] = (c[2 * j] | (c[2 * j + 1] << 16)) ^ flip;
+}
+
 // Sixteen BF16 values (8 words) -> sixteen E4M3 codes (one 16-byte chunk).
 __device__ __forceinline__ uint4 codes16(const uint32_t *w, const GroupScale &g)
 {
