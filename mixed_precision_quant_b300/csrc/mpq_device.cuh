@@ -483,7 +483,17 @@ __device__ __forceinline__ GroupScale make_group_scale(float amax, bool pow2)
         else { g.r = 0.0f; g.mode = 2; }
         return g;
     }
-    g.s = __fdiv_rn(amax, 448.0f);
+    // amax / 448 correctly rounded.  From 2^-100 up, the correction step below (the same
+    // as the elements' quotients', with the constant r = RN(1/448)) yields the IEEE
+    // quotient -- checked exhaustively on the CPU for every binary32 in [2^-100, max]
+    // against IEEE division; smaller max-abs values take the division itself.
+    if (amax >= 0x1p-100f) {
+        constexpr float r448 = 0x1.24924ap-9f;   // RN(1/448)
+        const float q0 = __fmul_rn(amax, r448);
+        g.s = __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), r448, q0);
+    } else {
+        g.s = __fdiv_rn(amax, 448.0f);
+    }
     if (g.s < kMinCorrectedScale) {
         g.s = fmaxf(g.s, 0x1p-149f);
         g.r = 0.0f; g.mode = 2;

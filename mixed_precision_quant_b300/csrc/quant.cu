@@ -461,14 +461,16 @@ cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream
 // a TMA ring.  Consumer thread (cp, qd) owns columns 2cp, 2cp+1 and rows 32qd .. +31 of the
 // tile: it reads code pairs with 2-byte shared loads (the two columns of one row,
 // conflict-free), keeps its 64 dequantized values in registers, and the four row quarters'
-// max-abs values meet in shared memory.  Each column's 32 codes go to the swizzled staging
-// tile as two 16-byte pieces of row c, which leaves with one TMA store per tile.  Two CTAs
-// share an SM, so one's tile latency (barriers, conversion) overlaps the other's.
+// max-abs values meet in shared memory (one CTA-wide barrier per tile; the partials are
+// double-buffered by tile parity).  Each column's 32 codes go to the swizzled staging tile
+// as two 16-byte pieces of row c; one thread waits for the eight warps' rows and issues the
+// tile's TMA store while the others move on.  Two CTAs share an SM, so one's tile latency
+// (barrier, conversion) overlaps the other's.
 constexpr int RQ_STAGES = 4;
 constexpr int kRqCtasPerSm = 2;
 constexpr uint32_t kRqScales = 128 * 4;   // one tile's row scales
 constexpr size_t kRqSmem =
-    1024 + RQ_STAGES * kBox + 2 * kBox + RQ_STAGES * kRqScales + 4 * 128 * 4 + (2 * RQ_STAGES + 2) * 8 + 16;
+    1024 + RQ_STAGES * kBox + 2 * kBox + RQ_STAGES * kRqScales + 2 * 4 * 128 * 4 + (2 * RQ_STAGES + 2) * 8 + 16;
 
 template <bool POW2>
 __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
@@ -480,16 +482,17 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad, out = stage + RQ_STAGES * kBox, scl = out + 2 * kBox;
     float *red = reinterpret_cast<float *>(smem_raw + pad + (RQ_STAGES + 2) * kBox + RQ_STAGES * kRqScales);
-    const uint32_t bars = smem_u32(red + 4 * 128);   // full[S], empty[S], syncA, syncB
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 4 * 128 + (2 * RQ_STAGES + 2) * 2);
-    const uint32_t full = bars, empty = bars + 8 * RQ_STAGES, syncA = bars + 16 * RQ_STAGES, syncB = syncA + 8;
+    // red: [2][4][128] partial max-abs values; then full[S], empty[S], syncA, ready, abort flag
+    const uint32_t bars = smem_u32(red + 2 * 4 * 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * 4 * 128 + (2 * RQ_STAGES + 2) * 2);
+    const uint32_t full = bars, empty = bars + 8 * RQ_STAGES, syncA = bars + 16 * RQ_STAGES, ready = syncA + 8;
     if (threadIdx.x == 0) {
         for (int i = 0; i < RQ_STAGES; ++i) {
             mbar_init(full + 8 * i, 1);
             mbar_init(empty + 8 * i, kConsumers);
         }
         mbar_init(syncA, kConsumers);
-        mbar_init(syncB, kConsumers);
+        mbar_init(ready, kConsumers);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -521,13 +524,16 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
     }
     const int cp = lane + 32 * (warp & 1), qd = warp >> 1, c = 2 * cp;
     const bool elected = threadIdx.x == 0;
-    uint32_t kA = 0, kB = 0, it = 0;
+    // byte offset of this thread's code pair in a row r of a swizzled tile: chunk cp/8 sits
+    // at chunk (cp/8) ^ (r % 8)
+    const uint32_t chunk16 = (cp >> 3) << 4, byte_in = (2 * cp) & 15;
+    uint32_t kA = 0, it = 0;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         const int64_t tb = item / ncb, cb = item - tb * ncb;
         const uint32_t st = it % RQ_STAGES, ph = (it / RQ_STAGES) & 1;
         if (!mbar_wait(full + 8 * st, ph, ctl, 0x1810 | st))
             break;
-        const uint32_t tile = stage + st * kBox;
+        const uint32_t tile = stage + st * kBox + 32 * 128 * qd;   // row 32qd of the tile
         float sc[32];   // input scales of rows 32qd .. +31 (the same for every lane: broadcast)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -537,27 +543,32 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
         }
         float xa[32], xb[32], ma = 0.0f, mb = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int t = 32 * qd + i;
-            const uint32_t pair = lds_u16(tile + sw128(t, cp >> 3) + ((2 * cp) & 15));
-            const __half2 h(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3));
-            const float2 d = __half22float2(h);   // exact: every E4M3 value is an FP16 value
-            xa[i] = __fmul_rn(d.x, sc[i]);        // column c (the pair's low byte)
-            xb[i] = __fmul_rn(d.y, sc[i]);        // column c + 1
-            ma = fmaxf(ma, fabsf(xa[i]));
-            mb = fmaxf(mb, fabsf(xb[i]));
+        for (int k = 0; k < 8; ++k) {   // rows 32qd + k + 8m share the swizzle phase k
+            const uint32_t rowk = tile + (chunk16 ^ (k << 4)) + byte_in + 128 * k;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int i = k + 8 * m;
+                const uint32_t pair = lds_u16(rowk + 1024 * m);
+                const __half2 h(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3));
+                const float2 d = __half22float2(h);   // exact: every E4M3 value is an FP16 value
+                xa[i] = __fmul_rn(d.x, sc[i]);        // column c (the pair's low byte)
+                xb[i] = __fmul_rn(d.y, sc[i]);        // column c + 1
+                ma = fmaxf(ma, fabsf(xa[i]));
+                mb = fmaxf(mb, fabsf(xb[i]));
+            }
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(empty + 8 * st);
-        *reinterpret_cast<float2 *>(red + qd * 128 + c) = make_float2(ma, mb);
+        float *redt = red + (it & 1) * 512;
+        *reinterpret_cast<float2 *>(redt + qd * 128 + c) = make_float2(ma, mb);
         if (elected)
             bulk_wait_read1();   // the store of two tiles ago has left this tile's staging buffer
         if (!wg_sync(syncA, kA, ctl, 0x1820))
             break;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float2 v = *reinterpret_cast<const float2 *>(red + q * 128 + c);
+            const float2 v = *reinterpret_cast<const float2 *>(redt + q * 128 + c);
             ma = fmaxf(ma, v.x);
             mb = fmaxf(mb, v.y);
         }
@@ -576,9 +587,12 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
             dst[0] = ga.s;
             dst[1] = gb.s;
         }
-        if (!wg_sync(syncB, kB, ctl, 0x1821))
-            break;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(ready);   // this warp's staging rows are written
         if (elected) {
+            if (!mbar_wait(ready, it & 1, ctl, 0x1821))
+                break;
             tma_store_2d(&tmqT, stg, static_cast<int32_t>(tb * 128), static_cast<int32_t>(cb * 128));
             bulk_commit();
         }
