@@ -541,7 +541,10 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
             sc[4 * j] = __uint_as_float(v.x); sc[4 * j + 1] = __uint_as_float(v.y);
             sc[4 * j + 2] = __uint_as_float(v.z); sc[4 * j + 3] = __uint_as_float(v.w);
         }
-        float xa[32], xb[32], ma = 0.0f, mb = 0.0f;
+        // P[i] = (column c, column c + 1) of row 32qd + i, dequantized: the pair's low and
+        // high byte times the row's scale, kept packed for the pairwise arithmetic below
+        unsigned long long P[32];
+        float ma = 0.0f, mb = 0.0f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {   // rows 32qd + k + 8m share the swizzle phase k
             const uint32_t rowk = tile + (chunk16 ^ (k << 4)) + byte_in + 128 * k;
@@ -551,10 +554,9 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
                 const uint32_t pair = lds_u16(rowk + 1024 * m);
                 const __half2 h(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3));
                 const float2 d = __half22float2(h);   // exact: every E4M3 value is an FP16 value
-                xa[i] = __fmul_rn(d.x, sc[i]);        // column c (the pair's low byte)
-                xb[i] = __fmul_rn(d.y, sc[i]);        // column c + 1
-                ma = fmaxf(ma, fabsf(xa[i]));
-                mb = fmaxf(mb, fabsf(xb[i]));
+                P[i] = fmul2(pack2(d.x, d.y), pack2(sc[i], sc[i]));
+                ma = fmaxf(ma, fabsf(lo_of(P[i])));
+                mb = fmaxf(mb, fabsf(hi_of(P[i])));
             }
         }
         __syncwarp();
@@ -573,9 +575,35 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
             mb = fmaxf(mb, v.y);
         }
         const GroupScale ga = make_group_scale(ma, POW2), gb = make_group_scale(mb, POW2);
+        // Codes of both columns per row with per-lane scales; four rows' code pairs are then
+        // regrouped by byte permutes into one word of column c and one of column c + 1.
         uint32_t wa[8], wb[8];
-        codes_f32<32>(xa, ga, wa);
-        codes_f32<32>(xb, gb, wb);
+        if (POW2 ? (ga.mode == 1 && gb.mode == 1) : (ga.mode != 2 && gb.mode != 2)) {
+            // amax/448 scales: the correction-step quotient (valid for the all-zero group's
+            // s = r = 1 as well); power-of-2 scales: the exact product by 2^-e
+            const unsigned long long nr = pack2(-ga.r, -gb.r), s2 = pack2(ga.s, gb.s), r2 = pack2(ga.r, gb.r);
+            const uint32_t flip = POW2 ? 0u : 0x80808080u;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const unsigned long long t = POW2 ? fmul2(P[4 * q + u], r2) : neg_quotient2(P[4 * q + u], nr, s2);
+                    v[u] = e4m3x2(lo_of(t), hi_of(t));   // low byte: column c
+                }
+                const uint32_t A = v[0] | (v[1] << 16), B = v[2] | (v[3] << 16);
+                wa[q] = __byte_perm(A, B, 0x6420) ^ flip;
+                wb[q] = __byte_perm(A, B, 0x7531) ^ flip;
+            }
+        } else {   // a tiny scale (IEEE division) in either column: element by element
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                wa[q] = e4m3_pair(lo_of(P[4 * q]), lo_of(P[4 * q + 1]), ga) |
+                        (e4m3_pair(lo_of(P[4 * q + 2]), lo_of(P[4 * q + 3]), ga) << 16);
+                wb[q] = e4m3_pair(hi_of(P[4 * q]), hi_of(P[4 * q + 1]), gb) |
+                        (e4m3_pair(hi_of(P[4 * q + 2]), hi_of(P[4 * q + 3]), gb) << 16);
+            }
+        }
         const uint32_t stg = out + (it & 1) * kBox;
         sts_v4(stg + sw128(c, 2 * qd), make_uint4(wa[0], wa[1], wa[2], wa[3]));
         sts_v4(stg + sw128(c, 2 * qd + 1), make_uint4(wa[4], wa[5], wa[6], wa[7]));
