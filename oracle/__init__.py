@@ -67,6 +67,12 @@ def _load():
         lib.mpqo_quant_tile_128x1.argtypes = [P, I, I, I, P, I, P, I, ctypes.c_int]
         lib.mpqo_quant_block_128x128.restype = None
         lib.mpqo_quant_block_128x128.argtypes = [P, I, I, I, P, I, P, I, P, I, ctypes.c_int]
+        lib.mpqo_exp_f32.restype = ctypes.c_float
+        lib.mpqo_exp_f32.argtypes = [ctypes.c_float]
+        lib.mpqo_silu_f32.restype = ctypes.c_float
+        lib.mpqo_silu_f32.argtypes = [ctypes.c_float]
+        lib.mpqo_swiglu_quant_1x128.restype = None
+        lib.mpqo_swiglu_quant_1x128.argtypes = [P, I, I, I, P, I, P, I, ctypes.c_int]
         lib.mpqo_requant_tile_128x1.restype = None
         lib.mpqo_requant_tile_128x1.argtypes = [P, I, I, I, P, I, P, I, P, I, ctypes.c_int]
         lib.mpqo_gemm_ref.restype = None
@@ -147,6 +153,33 @@ def quant_tile_128x1(x_bf16_bits: np.ndarray, pow2: bool = False):
     sT = np.empty((rows // 128, cols), np.float32)
     _load().mpqo_quant_tile_128x1(_ptr(x), rows, cols, cols, _ptr(qT), rows, _ptr(sT), cols, int(pow2))
     return qT, sT
+
+
+def exp_f32(x) -> np.ndarray:
+    """The path's binary32 exponential (Cody-Waite reduction + degree-7 Taylor), elementwise."""
+    lib = _load()
+    x = np.asarray(x, np.float32)
+    return np.array([lib.mpqo_exp_f32(float(v)) for v in x.ravel()], np.float32).reshape(x.shape)
+
+
+def silu_f32(x) -> np.ndarray:
+    lib = _load()
+    x = np.asarray(x, np.float32)
+    return np.array([lib.mpqo_silu_f32(float(v)) for v in x.ravel()], np.float32).reshape(x.shape)
+
+
+def swiglu_quant_1x128(hcat_bf16_bits: np.ndarray, pow2: bool = True):
+    """SwiGLU of [rows, 2W] BF16 (gate | up) and the 1x128 quantization of the result.
+
+    Returns (q uint8 [rows, W], s float32 [W/128, rows])."""
+    h = _c(hcat_bf16_bits, np.uint16)
+    rows, w2 = h.shape
+    assert w2 % 256 == 0
+    w = w2 // 2
+    q = np.empty((rows, w), np.uint8)
+    s = np.empty((w // 128, rows), np.float32)
+    _load().mpqo_swiglu_quant_1x128(_ptr(h), rows, w, w2, _ptr(q), w, _ptr(s), rows, int(pow2))
+    return q, s
 
 
 def requant_tile_128x1(q: np.ndarray, s: np.ndarray, pow2: bool = False):

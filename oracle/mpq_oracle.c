@@ -227,6 +227,82 @@ void mpqo_requant_tile_128x1(const uint8_t *q, int64_t rows, int64_t cols, int64
     }
 }
 
+/* ------------------------------------------- SwiGLU feeding the down projection */
+
+/* exp(x) in binary32 by Cody and Waite's argument reduction (W. J. Cody, W. Waite,
+ * "Software Manual for the Elementary Functions", 1980): n = rint(x log2 e),
+ * r = x - n ln2 with ln2 split into a 15-bit head (n * head is exact) and a tail, then the
+ * degree-7 Taylor polynomial of e^r (|r| <= ln2/2, truncation error below 2^-27) in Horner
+ * form with fused multiply-adds, scaled by 2^n.  This exact sequence of binary32 operations
+ * is the definition the GPU path follows; its accuracy against the true exponential is
+ * pinned by the tests (within 2 ulp).  x is clamped to [-104, 89]: below, e^x rounds to 0;
+ * above, it overflows to infinity, as it does after the clamp. */
+float mpqo_exp_f32(float x)
+{
+    const float l2e = 0x1.715476p+0f, ln2_hi = 0x1.62e4p-1f, ln2_lo = 0x1.7f7d1cp-20f;
+    if (x < -104.0f)
+        x = -104.0f;
+    if (x > 89.0f)
+        x = 89.0f;
+    const float nf = nearbyintf(x * l2e); /* ties to even */
+    const int n = (int)nf;
+    float r = fmaf(-nf, ln2_hi, x);
+    r = fmaf(-nf, ln2_lo, r);
+    float p = 0x1.a01a02p-13f;            /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);      /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);       /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);       /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);       /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    /* p * 2^n, with one rounding: the first factor below is exact */
+    if (n > 127)
+        return (p * 0x1p64f) * ldexpf(1.0f, n - 64);
+    if (n < -126)
+        return (p * ldexpf(1.0f, n + 64)) * 0x1p-64f;
+    return p * ldexpf(1.0f, n);
+}
+
+/* silu(g) = g / (1 + e^-g): one binary32 addition and one IEEE division. */
+float mpqo_silu_f32(float g)
+{
+    const float den = 1.0f + mpqo_exp_f32(-g);
+    return g / den;
+}
+
+/* SwiGLU of the up-projection output and its 1x128 quantization, the input of the down
+ * projection.  Page 1, first paragraph: the SwiGLU operator's inputs are cached and its
+ * output recomputed in the backward pass; page 4, second paragraph: the activation before
+ * the MoE down projection uses integral power-of-2 scales.
+ * hcat[r, 0 .. W) is the gate, hcat[r, W .. 2W) the up value (BF16 bits, ldh >= 2W);
+ * x[r, c] = silu(gate[r, c]) * up[r, c] (binary32, one rounded product); its 1x128 groups
+ * are quantized like mpqo_quant_tile_1x128's: q[r, c] (ldq), s[(c/128) * lds + r]. */
+void mpqo_swiglu_quant_1x128(const uint16_t *hcat, int64_t rows, int64_t width, int64_t ldh, uint8_t *q,
+                             int64_t ldq, float *s, int64_t lds, int pow2)
+{
+    int64_t nkb = width / 128;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            float x[128];
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                const int64_t c = kb * 128 + i;
+                const float g = bf16_to_float(hcat[r * ldh + c]);
+                const float u = bf16_to_float(hcat[r * ldh + width + c]);
+                x[i] = mpqo_silu_f32(g) * u;
+                float a = fabsf(x[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            float sc = mpqo_group_scale(amax, pow2);
+            s[kb * lds + r] = sc;
+            for (int i = 0; i < 128; ++i)
+                q[r * ldq + kb * 128 + i] = quant_one(x[i], sc);
+        }
+    }
+}
+
 /* 128x128 blocks: block (i, j) = w[i*128 .. +127, j*128 .. +127].
  * q[r, c] (ldq); optional transposed codes qT[c, r] (ldqT); s[i * lds + j]. */
 void mpqo_quant_block_128x128(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw,

@@ -450,3 +450,97 @@ def test_requant_zero_and_signed_zero_groups():
     assert np.all(sT == 1.0)
     assert np.all(qT[:128] == 0) and np.all(qT[128:] == 0x80)
 
+
+
+# ------------------------------------------------------ SwiGLU + quantization
+
+def _ulp32(v):
+    """Spacing of binary32 numbers at |v| (2^-149 in the subnormal range)."""
+    v = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -126)))
+    return 2.0 ** (e - 23)
+
+
+def test_exp_within_two_ulp_of_the_true_exponential():
+    rng = np.random.default_rng(50)
+    x = np.concatenate([rng.uniform(-103.0, 88.7, 200000), rng.uniform(-1, 1, 20000),
+                        np.linspace(-0.4, 0.4, 4001)]).astype(np.float32)
+    got = oracle.exp_f32(x).astype(np.float64)
+    true = np.exp(x.astype(np.float64))
+    assert np.all(np.abs(got - true) <= 2 * _ulp32(true))
+    assert oracle.exp_f32(np.float32(0.0)) == 1.0
+    assert oracle.exp_f32(np.float32(-104.5)) == 0.0 and oracle.exp_f32(np.float32(-1e30)) == 0.0
+    assert np.isinf(oracle.exp_f32(np.float32(89.0))) and np.isinf(oracle.exp_f32(np.float32(3e38)))
+
+
+def test_silu_close_to_the_true_function():
+    rng = np.random.default_rng(51)
+    # below about -88.7, e^-g overflows binary32 and the formula gives -0 (checked below)
+    g = np.concatenate([rng.standard_normal(100000) * 4, rng.uniform(-88, 90, 20000)]).astype(np.float32)
+    got = oracle.silu_f32(g).astype(np.float64)
+    gd = g.astype(np.float64)
+    true = gd / (1.0 + np.exp(-gd))
+    assert np.all(np.abs(got - true) <= 4 * _ulp32(true) + 2.0 ** -149)
+    # large positive g: e^-g is below half an ulp of 1, so silu(g) == g exactly
+    big = np.float32([17.0, 100.0, 3e38])
+    assert np.array_equal(oracle.silu_f32(big), big)
+    # large negative g: e^-g overflows, silu(g) == -0
+    neg = oracle.silu_f32(np.float32([-90.0, -3e38]))
+    assert np.all(neg == 0) and np.all(np.signbit(neg))
+
+
+def _bf16_trunc(x):
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_swiglu_quant_reduces_to_the_tile_quantizer(pow2):
+    """With gate >= 17 silu is the identity, and with up = +-2^k the product is exact and a
+    BF16 value: the SwiGLU quantizer must equal the 1x128 quantizer of gate * up."""
+    rng = np.random.default_rng(52)
+    rows, w = 64, 384
+    gate = rng.uniform(17, 3000, (rows, w)).astype(np.float32)
+    gate = ((_bf16_trunc(gate).astype(np.uint32) << 16).view(np.float32))
+    up = (rng.choice([-1.0, 1.0], (rows, w)) * 2.0 ** rng.integers(-20, 10, (rows, w))).astype(np.float32)
+    hcat = np.concatenate([_bf16_trunc(gate), _bf16_trunc(up)], axis=1)
+    q, s = oracle.swiglu_quant_1x128(hcat, pow2=pow2)
+    prod = (gate * up).astype(np.float32)
+    q2, s2 = oracle.quant_tile_1x128(bf16_bits(prod), pow2=pow2)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+
+
+def test_swiglu_quant_zero_groups_and_signs():
+    """gate = 0 or up = 0, or a very negative gate, give +-0 products: zero groups, scale 1,
+    codes carrying the product's sign."""
+    rows, w = 4, 128
+    gate = np.zeros((rows, w), np.float32)
+    up = np.ones((rows, w), np.float32)
+    gate[1] = -200.0                     # silu = -0, times +1 -> -0
+    up[2] = -1.0                         # +0 * -1 -> -0
+    gate[3] = 5.0; up[3] = 0.0           # silu(5) * +0 -> +0
+    hcat = np.concatenate([_bf16_trunc(gate), _bf16_trunc(up)], axis=1)
+    q, s = oracle.swiglu_quant_1x128(hcat, pow2=True)
+    assert np.all(s == 1.0)
+    assert np.all(q[0] == 0) and np.all(q[1] == 0x80) and np.all(q[2] == 0x80) and np.all(q[3] == 0)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_swiglu_quant_error_bound(pow2):
+    """Against silu(gate) * up in float64: the 1x128 quantization error bound (2^-4 relative
+    in the E4M3 normal range, 2^-10 s below it) plus the binary32 SwiGLU's own few ulps."""
+    rng = np.random.default_rng(53)
+    rows, w = 128, 512
+    gate = (rng.standard_normal((rows, w)) * 3).astype(np.float32)
+    up = (rng.standard_normal((rows, w)) * np.exp(rng.uniform(-5, 5, (rows, 1)))).astype(np.float32)
+    hcat = np.concatenate([_bf16_trunc(gate), _bf16_trunc(up)], axis=1)
+    g = (hcat[:, :w].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    u = (hcat[:, w:].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    x = g / (1.0 + np.exp(-g)) * u
+    q, s = oracle.swiglu_quant_1x128(hcat, pow2=pow2)
+    srow = np.repeat(s.T.astype(np.float64), 128, axis=1)
+    err = np.abs(torch_decode(q) * srow - x)
+    y = np.abs(x) / srow
+    normal = y >= 2.0 ** -6
+    slack = 1 + 2.0 ** -18
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(x[normal]) * slack + 8 * _ulp32(x[normal]))
+    assert np.all(err[~normal] <= 2.0 ** -10 * srow[~normal] * slack + 8 * _ulp32(x[~normal]))
