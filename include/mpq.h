@@ -182,6 +182,29 @@ mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, 
                                   int64_t ldsT, uint32_t flags, void *stream);
 
 /*
+ * fp8_swiglu_quant_1x128 -- SwiGLU of the MoE up-projection output fused with the 1x128
+ * quantization of the result, the FP8 input of the down projection (page 1, first
+ * paragraph: the SwiGLU output is recomputed from its cached inputs; page 4, second
+ * paragraph: this activation uses integral power-of-2 scales, flag MPQ_POW2).
+ *
+ *   hcat [rows, 2*width] BF16, ldh >= 2*width: hcat[r, c] is the gate and hcat[r, width + c]
+ *        the up value of output element (r, c) (device, read only);
+ *   q    [rows, width] E4M3, ldq >= width (device, written);
+ *   s    [width/128][lds] float32, lds >= rows: s[kb*lds + r] scales q[r, kb*128 .. +127].
+ *   flags: MPQ_POW2 (the pages' rule for this activation) or 0 (amax/448).
+ * x = silu(g) * u with silu(g) = g / (1 + e^-g), every operation in binary32 with one
+ * rounding; e^x is a fixed operation sequence (Cody-Waite reduction, degree-7 Taylor
+ * polynomial by fused multiply-adds, scaled by 2^n with one rounding; within 2 ulp of the
+ * true exponential), so results are reproducible bit for bit.  Where e^-g overflows
+ * (g below about -88.7) silu gives -0.  The groups of x are quantized as
+ * fp8_quant_tile_1x128 quantizes its groups; every product x must be finite.
+ * Requirements: width % 128 == 0, rows >= 0; hcat, q 16-byte aligned; ldh % 8 == 0;
+ * ldq % 16 == 0; s 4-byte aligned.  Asynchronous on `stream`; nothing is allocated.
+ */
+mpq_status fp8_swiglu_quant_1x128(mpq_handle h, const void *hcat, int64_t rows, int64_t width, int64_t ldh,
+                                  uint8_t *q, int64_t ldq, float *s, int64_t lds, uint32_t flags, void *stream);
+
+/*
  * fp8_quant_block_128x128 -- weight quantization in 128x128 blocks (page 1, second
  * paragraph: weights are quantized online from their max-abs value), optionally also
  * writing the transposed codes (same scales) used as the Dgrad B operand.

@@ -55,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "fp8_quant_tile_1x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, P, I, U32, P]),
         "fp8_quant_block_128x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
         "fp8_requant_tile_128x1": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
+        "fp8_swiglu_quant_1x128": (INT, [P, P, I, I, I, P, I, P, I, U32, P]),
         "fp8_gemm_blockscaled": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
         "fp8_grouped_gemm_blockscaled": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, U32, P]),
         "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
@@ -148,6 +149,23 @@ def fp8_quant_tile_1x128(x: torch.Tensor, *, pow2: bool = False, rows_out: bool 
                                    _stream(dev, stream))
     _check("fp8_quant_tile_1x128", st)
     return q, s, qT, sT
+
+
+def fp8_swiglu_quant_1x128(hcat: torch.Tensor, *, pow2: bool = True, q=None, s=None, stream=None):
+    """SwiGLU of the up-projection output ``hcat [rows, 2*width]`` BF16 (gate in the first
+    ``width`` columns, up in the rest) fused with the 1x128 quantization of
+    ``silu(gate) * up``.  Returns ``(q [rows, width] uint8, s [width/128, rows] float32)``;
+    ``pow2`` selects power-of-2 scales (the pages' rule for this activation)."""
+    _cuda2d(hcat, torch.bfloat16, "hcat")
+    rows, w2 = hcat.shape
+    width = w2 // 2
+    dev = hcat.device
+    q = q if q is not None else torch.empty((rows, width), dtype=torch.uint8, device=dev)
+    s = s if s is not None else torch.empty((width // 128, rows), dtype=torch.float32, device=dev)
+    st = _lib.fp8_swiglu_quant_1x128(_handle(dev), _ptr(hcat), rows, width, _ld(hcat), _ptr(q), _ld(q), _ptr(s),
+                                     _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
+    _check("fp8_swiglu_quant_1x128", st)
+    return q, s
 
 
 def fp8_requant_tile_128x1(q: torch.Tensor, s: torch.Tensor, *, pow2: bool = False, qT=None, sT=None,

@@ -282,6 +282,31 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
     return from_cuda(mpq::launch_quant_dual(tmx, tmq, tmqT, a, pow2, h->num_sms, st));
 }
 
+mpq_status fp8_swiglu_quant_1x128(mpq_handle h, const void *hcat, int64_t rows, int64_t width, int64_t ldh,
+                                  uint8_t *q, int64_t ldq, float *s, int64_t lds, uint32_t flags, void *stream)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if (flags & ~MPQ_POW2)
+        return MPQ_ERR_UNSUPPORTED;
+    if (rows < 0 || width <= 0 || width % 128 != 0 || ldh < 2 * width || ldq < width || lds < rows)
+        return MPQ_ERR_SHAPE;
+    if (rows == 0)   // nothing is read or written
+        return MPQ_OK;
+    if (hcat == nullptr || q == nullptr || s == nullptr)
+        return MPQ_ERR_NULL;
+    if (!aligned(hcat, 16) || ldh % 8 != 0 || !aligned(q, 16) || ldq % 16 != 0 || !aligned(s, 4))
+        return MPQ_ERR_ALIGN;
+    if (rows > (int64_t(1) << 31) || width > (int64_t(1) << 30))
+        return MPQ_ERR_SHAPE;
+    mpq::SwigluArgs a{};
+    a.h = static_cast<const uint16_t *>(hcat);
+    a.rows = rows; a.width = width; a.ldh = ldh;
+    a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
+    return from_cuda(mpq::launch_swiglu_quant(a, (flags & MPQ_POW2) != 0, h->num_sms,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq,
                                   const float *s, int64_t lds, uint8_t *qT, int64_t ldqT, float *sT,
                                   int64_t ldsT, uint32_t flags, void *stream)

@@ -38,6 +38,18 @@ struct RequantArgs {
 cudaError_t launch_requant(const CUtensorMap &tmq, const CUtensorMap &tmqT, const RequantArgs &a, bool pow2,
                            int num_sms, cudaStream_t st);
 
+// SwiGLU of [rows, 2*width] BF16 (gate | up) and the 1x128 quantization of the result.
+struct SwigluArgs {
+    const uint16_t *h;        // BF16 bits [rows][ldh]: gate in columns [0, width), up in [width, 2 width)
+    int64_t rows, width, ldh;
+    uint8_t *q;               // [rows][ldq]
+    int64_t ldq;
+    float *s;                 // [width/128][lds]
+    int64_t lds;
+};
+
+cudaError_t launch_swiglu_quant(const SwigluArgs &a, bool pow2, int num_sms, cudaStream_t st);
+
 cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
                               int num_sms, cudaStream_t st);
 cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,

@@ -1,0 +1,176 @@
+// swiglu.cu -- SwiGLU of the up-projection output fused with the 1x128 quantization of the
+// result, the FP8 input of the MoE down projection.
+//
+// Method (source pages: page 1, first paragraph -- the SwiGLU operator's inputs are cached
+// and its output recomputed in the backward pass; page 4, second paragraph -- the
+// activation before the MoE down projection uses integral power-of-2 scaling factors):
+//   x[r, c] = silu(gate[r, c]) * up[r, c],  silu(g) = g / (1 + e^-g),
+// with the gate in the first W columns of each input row and the up value in the next W,
+// all in binary32 with one rounding per operation; then the 1x128 groups of x are quantized
+// with the arithmetic of the tile quantizer (quant_device.cuh).  e^x is a fixed sequence of
+// binary32 operations: Cody and Waite's reduction (W. J. Cody, W. Waite, "Software Manual
+// for the Elementary Functions", 1980) with a 15-bit head of ln 2, the degree-7 Taylor
+// polynomial of e^r in Horner form with fused multiply-adds, and a scaling by 2^n with one
+// rounding; every step uses an explicitly rounded intrinsic, so no contraction changes it.
+//
+// Design: memory-bound (4 bytes read, ~1 byte written per output value).  A grid-stride
+// loop over (row, 128-column group) items; eight consecutive lanes share a group, each
+// holding two 16-byte chunks of the gate and the matching two of the up half (coalesced
+// 128-byte pieces per load instruction), the group's max-abs combined by three shuffles.
+// Each lane keeps the next batch's loads in flight while it converts the current one.
+#include "mpq_internal.h"
+#include "mpq_device.cuh"
+#include "quant_device.cuh"
+
+namespace mpq {
+namespace {
+
+constexpr int kSwThreads = 256;
+constexpr int kSwLpg = 8;                  // lanes per group
+constexpr int kSwCpl = 16 / kSwLpg;        // 16-byte chunks per lane, per half
+constexpr int kSwU = 2;                    // groups per lane and batch
+
+// e^x0 and e^x1: clamp to [-104, 89] (below, e^x rounds to 0; above, it overflows),
+// n = rint(x log2 e) with ties to even, r = x - n ln2 with ln2 split into a 15-bit head
+// (n * head is exact) and a tail, the degree-7 Taylor polynomial of e^r in Horner form,
+// then p * 2^n with one rounding.  The multiply-adds run as packed FP32x2 operations, each
+// lane rounded exactly like a scalar fused multiply-add.
+__device__ __forceinline__ void exp_cw2(float x0, float x1, float &e0, float &e1)
+{
+    x0 = fminf(fmaxf(x0, -104.0f), 89.0f);
+    x1 = fminf(fmaxf(x1, -104.0f), 89.0f);
+    const unsigned long long x = pack2(x0, x1);
+    const unsigned long long t = fmul2(x, pack2(0x1.715476p+0f, 0x1.715476p+0f));
+    const float nf0 = rintf(lo_of(t)), nf1 = rintf(hi_of(t));
+    const unsigned long long nn = pack2(-nf0, -nf1);
+    unsigned long long r = ffma2(nn, pack2(0x1.62e4p-1f, 0x1.62e4p-1f), x);
+    r = ffma2(nn, pack2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f), r);
+    unsigned long long p = pack2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+    p = ffma2(p, r, pack2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = ffma2(p, r, pack2(0x1.111112p-7f, 0x1.111112p-7f));
+    p = ffma2(p, r, pack2(0x1.555556p-5f, 0x1.555556p-5f));
+    p = ffma2(p, r, pack2(0x1.555556p-3f, 0x1.555556p-3f));
+    p = ffma2(p, r, pack2(0.5f, 0.5f));
+    p = ffma2(p, r, pack2(1.0f, 1.0f));
+    p = ffma2(p, r, pack2(1.0f, 1.0f));
+    const int n[2] = {static_cast<int>(nf0), static_cast<int>(nf1)};
+    const float pv[2] = {lo_of(p), hi_of(p)};
+    float e[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (n[i] > 127)
+            e[i] = __fmul_rn(__fmul_rn(pv[i], 0x1p64f), exp2_int(n[i] - 64));
+        else if (n[i] < -126)
+            e[i] = __fmul_rn(__fmul_rn(pv[i], exp2_int(n[i] + 64)), 0x1p-64f);
+        else
+            e[i] = __fmul_rn(pv[i], exp2_int(n[i]));
+    }
+    e0 = e[0];
+    e1 = e[1];
+}
+
+// silu(g0) u0 and silu(g1) u1.
+__device__ __forceinline__ void swiglu2(float g0, float g1, float u0, float u1, float &v0, float &v1)
+{
+    float e0, e1;
+    exp_cw2(-g0, -g1, e0, e1);
+    v0 = __fmul_rn(__fdiv_rn(g0, __fadd_rn(1.0f, e0)), u0);
+    v1 = __fmul_rn(__fdiv_rn(g1, __fadd_rn(1.0f, e1)), u1);
+}
+
+template <bool POW2>
+__global__ void __launch_bounds__(kSwThreads) swiglu_quant_kernel(const SwigluArgs p)
+{
+    const int KB = static_cast<int>(p.width / 128);
+    const int64_t ngroups = p.rows * KB;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int lg = static_cast<int>(gtid % kSwLpg);
+    const int64_t slot = gtid / kSwLpg, nslot = static_cast<int64_t>(gridDim.x) * blockDim.x / kSwLpg;
+    const int64_t step = nslot * kSwU;
+    // loads of batch `base`: per group u, the lane's chunks lg + c*LPG of the gate and up halves
+    auto load = [&](int64_t base, uint4 (&gv)[kSwU][kSwCpl], uint4 (&uv)[kSwU][kSwCpl]) {
+#pragma unroll
+        for (int u = 0; u < kSwU; ++u) {
+            const int64_t gi = base + u * nslot + slot;
+            const bool ok = gi < ngroups;
+            const int64_t r = ok ? gi / KB : 0;
+            const int kb = ok ? static_cast<int>(gi - r * KB) : 0;
+            const uint4 *gp = reinterpret_cast<const uint4 *>(p.h + r * p.ldh + kb * 128);
+            const uint4 *up = reinterpret_cast<const uint4 *>(p.h + r * p.ldh + p.width + kb * 128);
+#pragma unroll
+            for (int c = 0; c < kSwCpl; ++c) {
+                gv[u][c] = ok ? __ldg(gp + lg + c * kSwLpg) : make_uint4(0, 0, 0, 0);
+                uv[u][c] = ok ? __ldg(up + lg + c * kSwLpg) : make_uint4(0, 0, 0, 0);
+            }
+        }
+    };
+    uint4 gv[kSwU][kSwCpl], uv[kSwU][kSwCpl];
+    load(0, gv, uv);
+    for (int64_t base = 0; base < ngroups; base += step) {   // trip count uniform over the grid
+        uint4 gn[kSwU][kSwCpl], un[kSwU][kSwCpl];
+        load(base + step, gn, un);
+#pragma unroll
+        for (int u = 0; u < kSwU; ++u) {
+            const int64_t gi = base + u * nslot + slot;
+            float x[8 * kSwCpl];
+            float m = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kSwCpl; ++c) {
+                const uint32_t gw[4] = {gv[u][c].x, gv[u][c].y, gv[u][c].z, gv[u][c].w};
+                const uint32_t uw[4] = {uv[u][c].x, uv[u][c].y, uv[u][c].z, uv[u][c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v0, v1;
+                    swiglu2(__uint_as_float(bf16x2_lo(gw[j])), __uint_as_float(bf16x2_hi(gw[j])),
+                            __uint_as_float(bf16x2_lo(uw[j])), __uint_as_float(bf16x2_hi(uw[j])), v0, v1);
+                    x[8 * c + 2 * j] = v0;
+                    x[8 * c + 2 * j + 1] = v1;
+                    m = fmaxf(m, fmaxf(fabsf(v0), fabsf(v1)));
+                }
+            }
+#pragma unroll
+            for (int o = kSwLpg / 2; o > 0; o >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (gi < ngroups) {
+                const int64_t r = gi / KB;
+                const int kb = static_cast<int>(gi - r * KB);
+                const GroupScale g = make_group_scale(m, POW2);
+                uint8_t *dst = p.q + r * p.ldq + kb * 128;
+#pragma unroll
+                for (int c = 0; c < kSwCpl; ++c) {
+                    uint32_t w[2];
+                    codes_f32<8>(&x[8 * c], g, w);
+                    *reinterpret_cast<uint2 *>(dst + (lg + c * kSwLpg) * 8) = make_uint2(w[0], w[1]);
+                }
+                if (lg == 0)
+                    p.s[static_cast<int64_t>(kb) * p.lds + r] = g.s;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kSwU; ++u)
+#pragma unroll
+            for (int c = 0; c < kSwCpl; ++c) {
+                gv[u][c] = gn[u][c];
+                uv[u][c] = un[u][c];
+            }
+    }
+}
+
+} // namespace
+
+cudaError_t launch_swiglu_quant(const SwigluArgs &a, bool pow2, int num_sms, cudaStream_t st)
+{
+    const int64_t ngroups = a.rows * (a.width / 128);
+    if (ngroups == 0)
+        return cudaSuccess;
+    const int64_t want = (ngroups * kSwLpg + kSwThreads - 1) / kSwThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    if (pow2)
+        swiglu_quant_kernel<true><<<grid, kSwThreads, 0, st>>>(a);
+    else
+        swiglu_quant_kernel<false><<<grid, kSwThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace mpq

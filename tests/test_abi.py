@@ -25,7 +25,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["fp8_quant_tile_1x128", "fp8_quant_block_128x128", "fp8_requant_tile_128x1", "fp8_gemm_blockscaled",
+    for n in ["fp8_quant_tile_1x128", "fp8_quant_block_128x128", "fp8_requant_tile_128x1", "fp8_swiglu_quant_1x128",
+              "fp8_gemm_blockscaled",
               "fp8_grouped_gemm_blockscaled", "mpq_version", "mpq_create", "mpq_destroy",
               "mpq_check_device_status"]:
         assert n in names, n
@@ -53,6 +54,8 @@ def test_null_handle_rejected_before_any_cuda_call(lib):
     I = ctypes.c_int64
     assert lib.fp8_requant_tile_128x1(P(0), P(0), I(128), I(128), I(128), P(0), I(128), P(0), I(128), P(0),
                                       I(128), ctypes.c_uint32(0), P(0)) == 1
+    assert lib.fp8_swiglu_quant_1x128(P(0), P(0), I(128), I(128), I(256), P(0), I(128), P(0), I(128),
+                                      ctypes.c_uint32(0), P(0)) == 1
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
