@@ -81,11 +81,14 @@ const char *mpq_version(void);
 /* Human-readable text of a status code (static storage). */
 const char *mpq_status_string(int status);
 
-/* Create a handle bound to the current CUDA device.  Allocates the 8-byte device
- * status word (cudaMalloc) and caches the SM count.  Not thread-safe per handle. */
+/* Create a handle bound to the current CUDA device.  Allocates (cudaMalloc, here and
+ * nowhere else) the 8-byte device status word and the stream-K handover area of the dense
+ * GEMM (128 KB per SM plus 32 bytes per SM of flags), and caches the SM count.  Not
+ * thread-safe per handle; dense GEMMs that take the stream-K schedule through one handle
+ * share its handover area and must not run concurrently (issue them on one stream). */
 mpq_status mpq_create(mpq_handle *out);
 
-/* Destroy a handle and free its status word.  Synchronizes the device first. */
+/* Destroy a handle and free its device memory.  Synchronizes the device first. */
 mpq_status mpq_destroy(mpq_handle h);
 
 /* Limit for every device-side wait launched through this handle, in nanoseconds
@@ -100,8 +103,20 @@ mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
  * pair tiles only when the experts average 2048 rows or more (each expert's rows are
  * rounded up to whole tiles, and a 256-row tile wastes more), else single-SM tiles.
  * mode 0: single-SM tiles everywhere.  mode 2: pair tiles everywhere.  Other values:
- * MPQ_ERR_UNSUPPORTED.  The tilings give bit-identical results. */
+ * MPQ_ERR_UNSUPPORTED.  The tilings give bit-identical results (with stream-K off). */
 mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
+
+/* Schedule of fp8_gemm_blockscaled through this handle (a throughput choice; the pages'
+ * method is the same).  Data-parallel: each CTA (pair) takes whole output tiles.  Stream-K:
+ * the 128-K slices of all tiles are split evenly over the CTAs (pairs); a tile shared by
+ * two of them is finished by the one holding its first slices, which adds the other's
+ * partial sum (FP32, through the handle's handover area) before the store, so the last
+ * wave has no idle SMs.  Results are deterministic for a given shape and device, and equal
+ * the data-parallel ones up to the FP32 rounding of that one addition per shared tile.
+ * mode 1 (default): stream-K when the tiles fill more than one wave and the last wave
+ * would leave more than a tenth of the machine idle; mode 0: never; mode 2: whenever the
+ * tiles fill more than one wave.  Other values: MPQ_ERR_UNSUPPORTED. */
+mpq_status mpq_set_gemm_stream_k(mpq_handle h, int mode);
 
 /*
  * mpq_set_workspace -- hands the handle a caller-owned device buffer for calls that need

@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
         "mpq_destroy": (INT, [P]),
         "mpq_set_wait_timeout": (INT, [P, U64]),
         "mpq_set_gemm_cta_pair": (INT, [P, INT]),
+        "mpq_set_gemm_stream_k": (INT, [P, INT]),
         "mpq_check_device_status": (INT, [P, P, ctypes.POINTER(INT)]),
         "fp8_quant_tile_1x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, P, I, U32, P]),
         "fp8_quant_block_128x128": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
@@ -351,6 +352,14 @@ def mpq_set_gemm_cta_pair(mode, device=None):
     tiles everywhere; 2 -- pair tiles everywhere."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     _check("mpq_set_gemm_cta_pair", _lib.mpq_set_gemm_cta_pair(_handle(dev), int(mode)))
+
+
+def mpq_set_gemm_stream_k(mode, device=None):
+    """Schedule of the dense GEMM: 1 (default) -- stream-K when the last wave of tiles would
+    leave more than a tenth of the SMs' time idle; 0 -- data-parallel whole tiles; 2 --
+    stream-K whenever the tiles fill more than one wave."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    _check("mpq_set_gemm_stream_k", _lib.mpq_set_gemm_stream_k(_handle(dev), int(mode)))
 
 
 def mpq_selftest_wait_timeout(timeout_ns: int = 1_000_000, device=None, stream=None):

@@ -17,6 +17,10 @@ struct mpq_handle_s {
     int pair_mode;          // 2-SM pair tiles: 0 never, 1 dense (+ grouped with large experts), 2 always
     void *workspace;        // caller-owned scratch (mpq_set_workspace), may be null
     size_t workspace_bytes;
+    int sk_mode;            // stream-K for dense GEMMs: 0 never, 1 when the last wave is short, 2 always
+    int sk_epoch;           // incremented per stream-K launch; flags equal to it are this launch's
+    int *d_sk_flags;        // [num_sms][8] handover flags
+    float4 *d_sk_part;      // [num_sms][8][32][32] handover partials (128 KB per SM)
 };
 
 namespace {
@@ -151,11 +155,23 @@ mpq_status mpq_create(mpq_handle *out)
         delete h;
         return MPQ_ERR_CUDA;
     }
-    if (cudaMemset(h->d_status, 0, 2 * sizeof(int)) != cudaSuccess) {
+    const size_t flag_bytes = static_cast<size_t>(h->num_sms) * 8 * sizeof(int);
+    const size_t part_bytes = static_cast<size_t>(h->num_sms) * 8 * 1024 * sizeof(float4);
+    if (cudaMemset(h->d_status, 0, 2 * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&h->d_sk_flags), flag_bytes) != cudaSuccess) {
         cudaFree(h->d_status);
         delete h;
         return MPQ_ERR_CUDA;
     }
+    if (cudaMemset(h->d_sk_flags, 0, flag_bytes) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&h->d_sk_part), part_bytes) != cudaSuccess) {
+        cudaFree(h->d_sk_flags);
+        cudaFree(h->d_status);
+        delete h;
+        return MPQ_ERR_CUDA;
+    }
+    h->sk_mode = 1;
+    h->sk_epoch = 0;
     h->timeout_ns = kDefaultTimeoutNs;
     h->pair_mode = 1;
     h->workspace = nullptr;
@@ -170,8 +186,10 @@ mpq_status mpq_destroy(mpq_handle h)
         return MPQ_ERR_NULL;
     cudaDeviceSynchronize();
     cudaError_t e = cudaFree(h->d_status);
+    const cudaError_t e2 = cudaFree(h->d_sk_flags);
+    const cudaError_t e3 = cudaFree(h->d_sk_part);
     delete h;
-    return from_cuda(e);
+    return from_cuda(e != cudaSuccess ? e : e2 != cudaSuccess ? e2 : e3);
 }
 
 mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns)
@@ -189,6 +207,16 @@ mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable)
     if (enable < 0 || enable > 2)
         return MPQ_ERR_UNSUPPORTED;
     h->pair_mode = enable;
+    return MPQ_OK;
+}
+
+mpq_status mpq_set_gemm_stream_k(mpq_handle h, int mode)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if (mode < 0 || mode > 2)
+        return MPQ_ERR_UNSUPPORTED;
+    h->sk_mode = mode;
     return MPQ_OK;
 }
 
@@ -433,6 +461,21 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     a.offsets = nullptr; a.G = 1;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
+    // Stream-K when the tiles fill more than one wave of CTAs (pairs) and, in the default
+    // mode, the last wave would leave more than a tenth of the machine's time idle.
+    const int64_t tile_m = pair ? 256 : 128;
+    const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + 255) / 256);
+    const int64_t units = pair ? h->num_sms / 2 : h->num_sms;
+    bool sk = false;
+    if (h->sk_mode != 0 && tiles > units) {
+        const int64_t waves = (tiles + units - 1) / units;
+        sk = h->sk_mode == 2 || 10 * (waves * units - tiles) > waves * units;
+    }
+    if (sk) {
+        a.sk_part = h->d_sk_part;
+        a.sk_flags = h->d_sk_flags;
+        a.sk_epoch = ++h->sk_epoch;
+    }
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, pair, h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }

@@ -101,6 +101,53 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     return true;
 }
 
+// Work order of one CTA (pair): whole tiles unit, unit + nunits, ... (data-parallel), or,
+// for stream-K, the contiguous run [unit U / nunits, (unit + 1) U / nunits) of the
+// U = T KB slices in tile-major order, cut into per-tile segments [kb0, kb1).  With
+// T >= nunits every run spans at least one tile, so a tile is shared by at most two
+// consecutive units: the later one computes its last slices first (a "tail" segment, the
+// run's first) and the earlier one its first slices last (a "head" segment, the run's last).
+struct Sched {
+    int64_t u, u1;     // stream-K position and end of the run
+    int t, T, KB, nunits;
+    bool sk;
+};
+
+__device__ __forceinline__ Sched sched_init(bool sk, int unit, int nunits, int T, int KB)
+{
+    Sched s;
+    const int64_t U = static_cast<int64_t>(T) * KB;
+    s.u = sk ? unit * U / nunits : 0;
+    s.u1 = sk ? (unit + 1) * U / nunits : 0;
+    s.t = unit;
+    s.T = T;
+    s.KB = KB;
+    s.nunits = nunits;
+    s.sk = sk;
+    return s;
+}
+
+__device__ __forceinline__ bool sched_next(Sched &s, int &t, int &kb0, int &kb1)
+{
+    if (s.sk) {
+        if (s.u >= s.u1)
+            return false;
+        t = static_cast<int>(s.u / s.KB);
+        kb0 = static_cast<int>(s.u - static_cast<int64_t>(t) * s.KB);
+        const int64_t left = s.u1 - s.u;
+        kb1 = left < s.KB - kb0 ? kb0 + static_cast<int>(left) : s.KB;
+        s.u += kb1 - kb0;
+        return true;
+    }
+    if (s.t >= s.T)
+        return false;
+    t = s.t;
+    kb0 = 0;
+    kb1 = s.KB;
+    s.t += s.nunits;
+    return true;
+}
+
 // acc[32 c + i] += partial column 32 c + i times its scales, for one 32-column chunk.
 // Scalar FMAs on purpose: the packed FP32x2 form runs on one of the SM's two FP32 pipes
 // only (four cycles per warp instruction), scalar FMAs use both -- half the pipe time for
@@ -119,7 +166,7 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
     }
 }
 
-template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE>
+template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs p, const FuseArgs f)
@@ -283,14 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
             uint32_t it = 0;
-            for (int t = unit; t < T; t += nunits) {
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
                 const Tile ti = tile_of(t);
                 if (FUSE) {   // the expert's token codes are complete (phase 1 of all CTAs)
                     if (!wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0180))
                         goto producer_done;
                     fence_proxy_async_global();
                 }
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(bar(C::BAR_DONE + s), ph ^ 1, ctl, 0x0100 | s))
                         goto producer_done;
@@ -329,8 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(smA));
             const uint64_t db0 = sdesc_kmajor_sw128(smem_u32(smB));
             uint32_t s = 0, ph = 0, buf = 0, tph = 0;
-            for (int t = unit; t < T; t += nunits) {
-                for (int kb = 0; kb < KB; ++kb) {
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(bar(C::BAR_TEMPTY + buf), tph ^ 1, ctl, 0x0200 | buf))
                         goto mma_done;
                     if (!mbar_wait(bar(C::BAR_FULL + s), ph, ctl, 0x0210 | s))
@@ -366,12 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 2) {
             // ---------------------------------------------------------- scale loader
             uint32_t it = 0;
-            for (int t = unit; t < T; t += nunits) {
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
                 const Tile ti = tile_of(t);
                 if (FUSE && !wait_count(f.ready + ti.g, goff[ti.g + 1] - goff[ti.g], ctl, 0x0380))
                     goto scale_done;
                 const float *sbg = p.sB + ti.sb_base;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const uint32_t j = it % SSLOTS, ph = (it / SSLOTS) & 1;
                     if (!mbar_wait(bar(C::BAR_SEMPTY + j), ph ^ 1, ctl, 0x0300 | j))
                         goto scale_done;
@@ -411,13 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tm_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = unit; t < T && ok; t += nunits) {
+        Sched sc = sched_init(SK, unit, nunits, T, KB);
+        int t, kb0, kb1;
+        while (ok && sched_next(sc, t, kb0, kb1)) {
             const Tile ti = tile_of(t);
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i)
                 acc[i] = 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const uint32_t j = it % SSLOTS, sph = (it / SSLOTS) & 1;
                 const uint32_t buf = it & 1;
                 const uint32_t ds = it % STAGES, dph = (it / STAGES) & 1;
@@ -462,6 +517,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
+            if (SK && kb0 > 0) {
+                // Tail of a tile the previous unit finishes: hand this warp's partial over
+                // (layout [unit][rank (pair mode)][warp][i][lane], coalesced) and announce it.
+                float4 *dst = p.sk_part + ((static_cast<int64_t>(unit) * (PAIR ? 2 : 1) + rank) * 8 + ew) * 1024 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    dst[32 * i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    asm volatile("st.release.gpu.global.s32 [%0], %1;"
+                                 ::"l"(p.sk_flags + (unit * (PAIR ? 2 : 1) + rank) * 8 + ew),
+                                 "r"(p.sk_epoch)
+                                 : "memory");
+                continue;
+            }
+            if (SK && kb1 < KB) {
+                // Head of a tile: add the tail the next unit computed (final sum: head + tail).
+                const int slot = ((unit + 1) * (PAIR ? 2 : 1) + static_cast<int>(rank)) * 8 + ew;
+                if (!wait_count(p.sk_flags + slot, p.sk_epoch, ctl, 0x0480)) {
+                    ok = false;
+                    break;
+                }
+                const float4 *src = p.sk_part + static_cast<int64_t>(slot) * 1024 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float4 v = __ldcg(src + 32 * i);
+                    acc[4 * i] = __fadd_rn(acc[4 * i], v.x);
+                    acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], v.y);
+                    acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], v.z);
+                    acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], v.w);
+                }
+            }
             // Output: rows [ti.row0 + 32 quad, +32), columns [ti.n0 + 128 half, +128).  A warp
             // whose 32 rows all belong to this tile stages 64-byte row pieces in its swizzled
             // 2 KB buffer and writes them with TMA stores (clipped at the tensor bounds);
@@ -572,11 +660,11 @@ __global__ void wait_selftest_kernel(int *status, uint64_t timeout_ns)
     }
 }
 
-template <int SB, bool F32, bool GR, bool PAIR, bool FUSE>
+template <int SB, bool F32, bool GR, bool PAIR, bool FUSE, bool SK>
 cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
                        const FuseArgs &f, int grid, cudaStream_t st)
 {
-    auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE>;
+    auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE, SK>;
     const size_t smem = smem_bytes<PAIR>(GR);
     static bool configured = false;  // one attribute call per instantiation and process
     if (!configured) {
@@ -644,21 +732,30 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
         cudaError_t e = cudaMemsetAsync(fuse->ready, 0, sizeof(int) * static_cast<size_t>(a.G), st);
         if (e != cudaSuccess)
             return e;
-        return out_fp32 ? launch_one<kScaleBlockNK, true, true, false, true>(tmA, tmB, tmC, a, *fuse, num_sms, st)
-                        : launch_one<kScaleBlockNK, false, true, false, true>(tmA, tmB, tmC, a, *fuse, num_sms, st);
+        return out_fp32 ? launch_one<kScaleBlockNK, true, true, false, true, false>(tmA, tmB, tmC, a, *fuse, num_sms, st)
+                        : launch_one<kScaleBlockNK, false, true, false, true, false>(tmA, tmB, tmC, a, *fuse, num_sms, st);
     }
-#define MPQ_G(SB, F32, GR, PR)                                                             \
-    if (scale_b == SB && out_fp32 == F32 && grouped == GR && pair == PR)                   \
-        return launch_one<SB, F32, GR, PR, false>(tmA, tmB, tmC, a, none, grid, st);
-#define MPQ_G2(SB, F32, GR) MPQ_G(SB, F32, GR, true) MPQ_G(SB, F32, GR, false)
-    MPQ_G2(kScaleBlockNK, false, false)
-    MPQ_G2(kScaleBlockNK, true, false)
-    MPQ_G2(kScaleBlockKN, false, false)
-    MPQ_G2(kScaleBlockKN, true, false)
-    MPQ_G2(kScaleRowKN, false, false)
-    MPQ_G2(kScaleRowKN, true, false)
-    MPQ_G2(kScaleBlockNK, false, true)
-    MPQ_G2(kScaleBlockNK, true, true)
+    const bool sk = a.sk_part != nullptr;
+    if (sk && (grouped || tiles < (pair ? grid / 2 : grid)))   // stream-K: dense, at least one wave
+        return cudaErrorInvalidValue;
+#define MPQ_G(SB, F32, GR, PR, SKV)                                                        \
+    if (scale_b == SB && out_fp32 == F32 && grouped == GR && pair == PR && sk == SKV)      \
+        return launch_one<SB, F32, GR, PR, false, SKV>(tmA, tmB, tmC, a, none, grid, st);
+#define MPQ_G2(SB, F32, GR, SKV) MPQ_G(SB, F32, GR, true, SKV) MPQ_G(SB, F32, GR, false, SKV)
+    MPQ_G2(kScaleBlockNK, false, false, false)
+    MPQ_G2(kScaleBlockNK, true, false, false)
+    MPQ_G2(kScaleBlockKN, false, false, false)
+    MPQ_G2(kScaleBlockKN, true, false, false)
+    MPQ_G2(kScaleRowKN, false, false, false)
+    MPQ_G2(kScaleRowKN, true, false, false)
+    MPQ_G2(kScaleBlockNK, false, false, true)
+    MPQ_G2(kScaleBlockNK, true, false, true)
+    MPQ_G2(kScaleBlockKN, false, false, true)
+    MPQ_G2(kScaleBlockKN, true, false, true)
+    MPQ_G2(kScaleRowKN, false, false, true)
+    MPQ_G2(kScaleRowKN, true, false, true)
+    MPQ_G2(kScaleBlockNK, false, true, false)
+    MPQ_G2(kScaleBlockNK, true, true, false)
 #undef MPQ_G2
 #undef MPQ_G
     return cudaErrorInvalidValue;

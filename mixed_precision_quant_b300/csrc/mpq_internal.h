@@ -73,6 +73,13 @@ struct GemmArgs {
     int G;                      // grouped: number of experts, else 1
     int *status;                // device status word (2 ints)
     uint64_t timeout_ns;
+    // Stream-K schedule (dense GEMMs): when sk_part is set, the 128-K slices of all tiles
+    // are split evenly over the CTAs (pairs); a tile begun by one and finished by the
+    // previous one is completed with the partial the first wrote into sk_part, announced
+    // by its sk_flags entries reaching sk_epoch.
+    float4 *sk_part;            // [units][2][8 warps][32][32] float4
+    int *sk_flags;              // [units][2][8 warps]
+    int sk_epoch;
 };
 
 // Fused activation quantization: the token rows come as BF16 x [M, K] (ldx elements) and

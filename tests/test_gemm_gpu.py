@@ -143,12 +143,62 @@ def test_pair_and_single_tiles_agree_bit_for_bit(mpq, op):
         qbT, sbT = oracle.quant_tile_128x1(bf16_bits(dy), pow2=True)
         args = (mpq.WGRAD, _dev(qaT), _dev(saT), _dev(qbT), _dev(sbT))
     outs = []
+    mpq.mpq_set_gemm_stream_k(0)
     for mode in (2, 0):
         mpq.mpq_set_gemm_cta_pair(mode)
         outs.append(mpq.fp8_gemm_blockscaled(*args, out_dtype=mpq.OUT_FP32))
     mpq.mpq_set_gemm_cta_pair(1)
+    mpq.mpq_set_gemm_stream_k(1)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
+
+
+# ------------------------------------------------------------------- stream-K
+
+@pytest.mark.parametrize("op", ["fprop", "wgrad"])
+def test_stream_k(mpq, tiles, op):
+    """Stream-K forced on 2560 x 2048 outputs with K = 1280 (80 pair tiles over 74 SM pairs,
+    160 single-SM tiles over 148 SMs: nearly every tile is shared by two units).  Sampled
+    outputs meet the oracle bound; every output is within FP32 rounding of the data-parallel
+    schedule's (a dropped or misplaced partial would not be); two runs agree bit for bit."""
+    M, N, K = 2560, 2048, 1280
+    if op == "fprop":
+        a = _bf16((M, K), 1.0, 21, outliers=0.01)
+        w = _bf16((N, K), 0.02, 22)
+        qa, sa = oracle.quant_tile_1x128(bf16_bits(a))
+        qb, _, sb = oracle.quant_block_128x128(bf16_bits(w))
+        o = oracle.FPROP
+        args = (mpq.FPROP, _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    else:
+        g = torch.Generator().manual_seed(23)
+        x = _bf16((K, M), 1.0, 24)                           # tokens x input features
+        dy = workloads.student_t3((K, N), 1e-3, g, "cpu")    # tokens x output features
+        qa, sa = oracle.quant_tile_128x1(bf16_bits(x))
+        qb, sb = oracle.quant_tile_128x1(bf16_bits(dy), pow2=True)
+        o = oracle.WGRAD
+        args = (mpq.WGRAD, _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    try:
+        mpq.mpq_set_gemm_stream_k(0)
+        dp = mpq.fp8_gemm_blockscaled(*args, out_dtype=mpq.OUT_FP32)
+        mpq.mpq_set_gemm_stream_k(2)
+        sk1 = mpq.fp8_gemm_blockscaled(*args, out_dtype=mpq.OUT_FP32)
+        sk2 = mpq.fp8_gemm_blockscaled(*args, out_dtype=mpq.OUT_FP32)
+        torch.cuda.synchronize()
+        st, where = mpq.mpq_check_device_status()
+        assert st == 0, (st, where)
+    finally:
+        mpq.mpq_set_gemm_stream_k(1)
+    assert torch.equal(sk1, sk2)
+    # every output: the two schedules sum the same slices in two orders (FP32 roundings only)
+    d = dp.double()
+    assert float((sk1.double() - d).abs().max()) <= 1e-5 * float(d.abs().max())
+    rng = np.random.default_rng(25)
+    ms = np.unique(np.concatenate([rng.integers(0, M, 40), [0, 255, 256, M - 1]])).astype(np.int64)
+    ns = np.unique(np.concatenate([rng.integers(0, N, 40), [0, 255, 256, N - 1]])).astype(np.int64)
+    mm, nn = np.meshgrid(ms, ns, indexing="ij")
+    ref, absref = oracle.gemm_ref_at(o, qa, sa, qb, sb, mm.ravel(), nn.ravel())
+    got = sk1.cpu().numpy().astype(np.float64)[mm.ravel(), nn.ravel()]
+    assert_gemm_close(got, ref, absref, f"stream-K {op}")
 
 
 # ------------------------------------------------------------ full-size samples
