@@ -238,21 +238,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // --------------------------------------------------- fused 1x128 + 128x1 (dual)
-constexpr int QD_STAGES = 2;
-
-// ------------------------------------------- fused 1x128 + 128x1, sixteen warps
 //
 // Row groups as in the row kernel, plus the 128x1 column groups written transposed (one
 // read of the tile for both).  One thread per group would need 64 words of data in
 // registers, which leaves room for eight consumer warps only, too few to hide the
 // latencies of a pass (shared loads, the max-abs tree, the scale's division).  Here each
 // thread owns half a group -- 64 values -- and the two halves' max-abs values meet in one
-// shuffle, so sixteen consumer warps fit.  Warps 8h .. 8h+7 own rows 128h .. +127 of the
-// tile; within them thread u (0..255) holds
+// shuffle, so sixteen consumer warps fit.  Tiles are 128 rows x 128 columns (32 KB of
+// BF16, two 128 x 64 TMA boxes) in a four-stage ring; warpgroup h (warps 8h .. 8h+7) takes
+// the CTA's tiles h, h+2, h+4, ..., so the two warpgroups run independently, each with its
+// own staging tiles and barrier.  Within a warpgroup thread u (0..255) holds
 //   row pass:    row u/2, columns 64 (u%2) .. +63;
-//   column pass: column u/2, rows 64 (u%2) .. +63 of the half.
+//   column pass: column u/2, rows 64 (u%2) .. +63.
+constexpr int QD_STAGES = 4;
+constexpr uint32_t kDualTile = 2 * kBox;          // 128 x 128 BF16
 constexpr int kDualConsumers = 16;
 constexpr int kDualThreads = 32 * (kDualConsumers + 1);
+constexpr size_t kDualSmem = 1024 + QD_STAGES * kDualTile + 4 * kBox + (2 * QD_STAGES + 2) * 8 + 16;
 
 template <bool POW2, bool ROWS>
 __global__ void __launch_bounds__(kDualThreads, 1)
@@ -260,47 +262,72 @@ __global__ void __launch_bounds__(kDualThreads, 1)
                         const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QSmem sm = q_carve<QD_STAGES, true>(smem_raw);
+    const uint32_t base0 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
+    const uint32_t stage = base0 + pad;
+    const uint32_t out_rows = stage + QD_STAGES * kDualTile, out_cols = out_rows + 2 * kBox;
+    const uint32_t bars = out_cols + 2 * kBox;        // full[S], empty[S], warpgroup[2]
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(smem_raw + pad + QD_STAGES * kDualTile + 4 * kBox + (2 * QD_STAGES + 2) * 8);
     if (threadIdx.x == 0) {
         for (int i = 0; i < QD_STAGES; ++i) {
-            mbar_init(sm.bars + 8 * i, 1);
-            mbar_init(sm.bars + 8 * (QD_STAGES + i), kDualConsumers);
+            mbar_init(bars + 8 * i, 1);
+            mbar_init(bars + 8 * (QD_STAGES + i), 8);   // the eight warps of one warpgroup
         }
-        mbar_init(sm.bars + 8 * (2 * QD_STAGES), 8);
-        mbar_init(sm.bars + 8 * (2 * QD_STAGES + 1), 8);
-        *sm.abort = 0;
+        mbar_init(bars + 8 * (2 * QD_STAGES), 8);
+        mbar_init(bars + 8 * (2 * QD_STAGES + 1), 8);
+        *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
-    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
-    const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
-    if (warp == kDualConsumers) {
-        if (lane == 0)
-            q_produce<QD_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+    const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;   // rows is a multiple of 128
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    if (warp == kDualConsumers) {   // producer: one 128-row tile as two 128 x 64 boxes
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+                const uint32_t st = it % QD_STAGES, ph = (it / QD_STAGES) & 1;
+                if (!mbar_wait(bars + 8 * (QD_STAGES + st), ph ^ 1, ctl, 0x1400 | st))
+                    break;
+                const int64_t rb = item / ncb, cb = item - rb * ncb;
+                mbar_arrive_expect_tx(bars + 8 * st, kDualTile);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+                    tma_load_2d(stage + st * kDualTile + b * kBox, &tmx, bars + 8 * st,
+                                static_cast<int32_t>(cb * 128 + b * 64), static_cast<int32_t>(rb * 128));
+            }
+            for (uint32_t j = it > QD_STAGES ? it - QD_STAGES : 0; j < it; ++j) {   // no load left in flight
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bars + 8 * (j % QD_STAGES), (j / QD_STAGES) & 1))
+                    if (globaltimer_ns() - t0 > p.timeout_ns)
+                        break;
+            }
+        }
         return;
     }
     const int h = t >> 8, u = t & 255;
     const int g2 = u >> 1, sub = u & 1;                    // group (row or column) and half
-    const uint32_t wgbar = sm.bars + 8 * (2 * QD_STAGES + h);
-    const uint32_t out_r = sm.out_rows + h * kBox, out_c = sm.out_cols + h * kBox;
+    const uint32_t wgbar = bars + 8 * (2 * QD_STAGES + h);
+    const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + h * kBox;
     const bool elected = u == 0;
-    uint32_t cph = 0, it = 0;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    uint32_t cph = 0;
+    uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
+    for (int64_t item = blockIdx.x + h * static_cast<int64_t>(gridDim.x); item < items;
+         item += 2 * static_cast<int64_t>(gridDim.x), it += 2) {
         const uint32_t st = it % QD_STAGES, ph = (it / QD_STAGES) & 1;
-        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1500 | st))
+        if (!mbar_wait(bars + 8 * st, ph, ctl, 0x1500 | st))
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
-        const uint32_t tile = sm.stage + st * kTile;
-        const int64_t y = rb * kTileRows + h * 128;       // first row of this half
-        const bool half_in = y < p.rows;                   // rows is a multiple of 128
+        const uint32_t tile = stage + st * kDualTile;
+        const int64_t y = rb * 128;                         // first row of the tile
         if (elected)
             bulk_wait_read0();                             // both staging boxes are free
         if (!wg_sync(wgbar, cph, ctl, 0x1510))
             break;
         uint32_t w[32];
         if (ROWS) {
-            const uint32_t box = tile + (h * 2 + sub) * kBox;   // rows of this half, columns 64 sub ..
+            const uint32_t box = tile + sub * kBox;          // columns 64 sub .. +63
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint4 v = lds_v4(box + sw128(g2, j));
@@ -309,14 +336,14 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             float a = amax_words(w);
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             const GroupScale g = make_group_scale(a, POW2);
-            if (half_in && sub == 0)
+            if (sub == 0)
                 p.s[cb * p.lds + y + g2] = g.s;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 sts_v4(out_r + sw128(g2, sub * 4 + q), codes16(&w[q * 8], g));
         }
         {
-            const uint32_t box = tile + (h * 2 + (g2 >> 6)) * kBox;
+            const uint32_t box = tile + (g2 >> 6) * kBox;
             const int j = (g2 & 63) >> 3, e = (g2 & 7) << 1;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -327,12 +354,12 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(sm.bars + 8 * (QD_STAGES + st));   // this warp has read the tile
+            mbar_arrive(bars + 8 * (QD_STAGES + st));      // this warp has read the tile
         {
             float a = amax_words(w);
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             const GroupScale g = make_group_scale(a, POW2);
-            if (half_in && sub == 0)
+            if (sub == 0)
                 p.sT[(y / 128) * p.ldsT + cb * 128 + g2] = g.s;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -341,7 +368,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         fence_proxy_async_smem();
         if (!wg_sync(wgbar, cph, ctl, 0x1511))
             break;
-        if (elected && half_in) {
+        if (elected) {
             if (ROWS)
                 tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
             tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
@@ -645,10 +672,10 @@ cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, co
 cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
                               const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
 {
-    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
+    const int64_t items = (a.rows / 128) * (a.cols / 128);   // rows is a multiple of 128 here
     if (items == 0)
         return cudaSuccess;
-    constexpr size_t smem = q_smem_bytes<QD_STAGES, true>();
+    constexpr size_t smem = kDualSmem;
     const bool rows_out = a.q != nullptr;
     if (pow2)
         return rows_out ? launch_q(quant_dual16_kernel<true, true>, smem, items, num_sms, st, kDualThreads, tmx, tmq,
