@@ -83,16 +83,16 @@ mpq_status encode_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t co
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
-// E4M3 code view [rows, cols] (cols contiguous), boxes of 128 rows x 128 bytes with 128-byte
+// E4M3 code view [rows, cols] (cols contiguous), boxes of box_rows rows x 128 bytes with 128-byte
 // swizzle (the quantizers' staging layout); stores are clipped at the tensor bounds.
-mpq_status encode_codes(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld)
+mpq_status encode_codes(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows = 128)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
         return MPQ_ERR_CUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -362,7 +362,7 @@ mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, 
     CUtensorMap tmq, tmqT;
     mpq_status e = encode_codes(&tmq, const_cast<uint8_t *>(q), rows, cols, ldq);
     if (e == MPQ_OK)
-        e = encode_codes(&tmqT, qT, cols, rows, ldqT);
+        e = encode_codes(&tmqT, qT, cols, rows, ldqT, 64);   // stored in 64-row halves
     if (e != MPQ_OK)
         return e;
     return from_cuda(mpq::launch_requant(tmq, tmqT, a, (flags & MPQ_POW2) != 0, h->num_sms,

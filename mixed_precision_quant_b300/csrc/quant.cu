@@ -488,16 +488,17 @@ cudaError_t launch_q(K kern, size_t smem, int64_t items, int num_sms, cudaStream
 // a TMA ring.  Consumer thread (cp, qd) owns columns 2cp, 2cp+1 and rows 32qd .. +31 of the
 // tile: it reads code pairs with 2-byte shared loads (the two columns of one row,
 // conflict-free), keeps its 64 dequantized values in registers, and the four row quarters'
-// max-abs values meet in shared memory (one CTA-wide barrier per tile; the partials are
-// double-buffered by tile parity).  Each column's 32 codes go to the swizzled staging tile
-// as two 16-byte pieces of row c; one thread waits for the eight warps' rows and issues the
-// tile's TMA store while the others move on.  Two CTAs share an SM, so one's tile latency
-// (barrier, conversion) overlaps the other's.
+// max-abs values meet in shared memory (the partials double-buffered by tile parity).  The
+// two column halves are independent: warps w, w+2, w+4, w+6 (w = 0, 1) own columns
+// 64w .. +63 and meet only among themselves, once per tile; each column's 32 codes go to
+// the swizzled staging tile as two 16-byte pieces of row c, and one thread per half waits
+// for its four warps' rows and issues that half's TMA store while the others move on.  Two
+// CTAs share an SM, so one's tile latency (barrier, conversion) overlaps the other's.
 constexpr int RQ_STAGES = 4;
 constexpr int kRqCtasPerSm = 2;
 constexpr uint32_t kRqScales = 128 * 4;   // one tile's row scales
 constexpr size_t kRqSmem =
-    1024 + RQ_STAGES * kBox + 2 * kBox + RQ_STAGES * kRqScales + 2 * 4 * 128 * 4 + (2 * RQ_STAGES + 2) * 8 + 16;
+    1024 + RQ_STAGES * kBox + 2 * kBox + RQ_STAGES * kRqScales + 2 * 4 * 128 * 4 + (2 * RQ_STAGES + 4) * 8 + 16;
 
 template <bool POW2>
 __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
@@ -509,17 +510,19 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad, out = stage + RQ_STAGES * kBox, scl = out + 2 * kBox;
     float *red = reinterpret_cast<float *>(smem_raw + pad + (RQ_STAGES + 2) * kBox + RQ_STAGES * kRqScales);
-    // red: [2][4][128] partial max-abs values; then full[S], empty[S], syncA, ready, abort flag
+    // red: [2][4][128] partial max-abs values; then full[S], empty[S], syncA[2], ready[2], abort
     const uint32_t bars = smem_u32(red + 2 * 4 * 128);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * 4 * 128 + (2 * RQ_STAGES + 2) * 2);
-    const uint32_t full = bars, empty = bars + 8 * RQ_STAGES, syncA = bars + 16 * RQ_STAGES, ready = syncA + 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * 4 * 128 + (2 * RQ_STAGES + 4) * 2);
+    const uint32_t full = bars, empty = bars + 8 * RQ_STAGES, syncA0 = bars + 16 * RQ_STAGES, ready0 = syncA0 + 16;
     if (threadIdx.x == 0) {
         for (int i = 0; i < RQ_STAGES; ++i) {
             mbar_init(full + 8 * i, 1);
             mbar_init(empty + 8 * i, kConsumers);
         }
-        mbar_init(syncA, kConsumers);
-        mbar_init(ready, kConsumers);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(syncA0 + 8 * h, kConsumers / 2);
+            mbar_init(ready0 + 8 * h, kConsumers / 2);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -549,8 +552,9 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
         }
         return;
     }
-    const int cp = lane + 32 * (warp & 1), qd = warp >> 1, c = 2 * cp;
-    const bool elected = threadIdx.x == 0;
+    const int half = warp & 1, cp = lane + 32 * half, qd = warp >> 1, c = 2 * cp;
+    const bool elected = lane == 0 && warp < 2;   // one storing thread per column half
+    const uint32_t syncA = syncA0 + 8 * half, ready = ready0 + 8 * half;
     // byte offset of this thread's code pair in a row r of a swizzled tile: chunk cp/8 sits
     // at chunk (cp/8) ^ (r % 8)
     const uint32_t chunk16 = (cp >> 3) << 4, byte_in = (2 * cp) & 15;
@@ -645,10 +649,11 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
         __syncwarp();
         if (lane == 0)
             mbar_arrive(ready);   // this warp's staging rows are written
-        if (elected) {
+        if (elected) {   // this half's 64 rows of the staging tile (rows of qT: columns of q)
             if (!mbar_wait(ready, it & 1, ctl, 0x1821))
                 break;
-            tma_store_2d(&tmqT, stg, static_cast<int32_t>(tb * 128), static_cast<int32_t>(cb * 128));
+            tma_store_2d(&tmqT, stg + half * 64 * 128, static_cast<int32_t>(tb * 128),
+                         static_cast<int32_t>(cb * 128 + 64 * half));
             bulk_commit();
         }
     }

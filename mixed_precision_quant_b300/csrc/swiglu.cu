@@ -14,9 +14,10 @@
 // rounding; every step uses an explicitly rounded intrinsic, so no contraction changes it.
 //
 // Design: memory-bound (4 bytes read, ~1 byte written per output value).  A grid-stride
-// loop over (row, 128-column group) items; eight consecutive lanes share a group, each
-// holding two 16-byte chunks of the gate and the matching two of the up half (coalesced
-// 128-byte pieces per load instruction), the group's max-abs combined by three shuffles.
+// loop over (row, 128-column group) items; four consecutive lanes share a group, each
+// holding four 16-byte chunks of the gate and the matching four of the up half (coalesced
+// 64-byte pieces per load instruction), the group's max-abs combined by two shuffles (eight
+// or sixteen lanes per group were slower: the per-group scale work is repeated per lane).
 // Each lane keeps the next batch's loads in flight while it converts the current one.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
@@ -26,9 +27,9 @@ namespace mpq {
 namespace {
 
 constexpr int kSwThreads = 256;
-constexpr int kSwLpg = 8;                  // lanes per group
+constexpr int kSwLpg = 4;                  // lanes per group
 constexpr int kSwCpl = 16 / kSwLpg;        // 16-byte chunks per lane, per half
-constexpr int kSwU = 2;                    // groups per lane and batch
+constexpr int kSwU = 1;                    // groups per lane and batch
 
 // e^x0 and e^x1: clamp to [-104, 89] (below, e^x rounds to 0; above, it overflows),
 // n = rint(x log2 e) with ties to even, r = x - n ln2 with ln2 split into a 15-bit head
