@@ -151,6 +151,24 @@ def profiled_traffic(name: str, digest: str):
         return None
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the default process group (x itself when there is no
+    group or a single rank): the job's time is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput of `world` independent replicas (weak scaling): the units all
+    ranks processed over the slowest rank's time, in units / 1e12 per second."""
+    return units_per_step * steps * world / (max_ms / 1e3) / 1e12
+
+
 def cpu_oracle_sample(rows=256, feats=2048):
     """Time the CPU oracle on a bounded sample of the dense Fprop workload: 1x128
     quantization of ``rows`` activation rows, 128x128 quantization of ``feats`` weight
@@ -241,13 +259,9 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [m[0].elapsed_time(m[3]) for m in marks]
     gemm_ms = [m[1].elapsed_time(m[2]) for m in marks]
     quant_ms = [m[0].elapsed_time(m[1]) for m in marks]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     flop_step = 2.0 * M * N * K
-    value = flop_step * args.steps * world / (total_ms / 1e3) / 1e12
+    value = replica_throughput(flop_step, args.steps, world, total_ms)
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     achieved = flop_step / (gemm_avg / 1e3) / 1e12
     traffic = profiled_traffic("gemm_dense_fprop_4096x18432x7168.txt", src_digest(GEMM_SOURCES))
