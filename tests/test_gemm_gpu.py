@@ -155,13 +155,14 @@ def test_pair_and_single_tiles_agree_bit_for_bit(mpq, op):
 
 # ------------------------------------------------------------------- stream-K
 
-@pytest.mark.parametrize("op", ["fprop", "wgrad"])
-def test_stream_k(mpq, tiles, op):
-    """Stream-K forced on 2560 x 2048 outputs with K = 1280 (80 pair tiles over 74 SM pairs,
-    160 single-SM tiles over 148 SMs: nearly every tile is shared by two units).  Sampled
+@pytest.mark.parametrize("op,M", [("fprop", 2560), ("wgrad", 2560), ("fprop", 2600)])
+def test_stream_k(mpq, tiles, op, M):
+    """Stream-K forced on M x 2048 outputs with K = 1280 (M = 2560: 80 pair tiles over 74 SM
+    pairs, 160 single-SM tiles over 148 SMs, so nearly every tile is shared by two units;
+    M = 2600 adds a ragged last row of tiles).  Sampled
     outputs meet the oracle bound; every output is within FP32 rounding of the data-parallel
     schedule's (a dropped or misplaced partial would not be); two runs agree bit for bit."""
-    M, N, K = 2560, 2048, 1280
+    N, K = 2048, 1280                  # M = 2600: the last row tiles are ragged
     if op == "fprop":
         a = _bf16((M, K), 1.0, 21, outliers=0.01)
         w = _bf16((N, K), 0.02, 22)
