@@ -381,10 +381,15 @@ __global__ void __launch_bounds__(kDualThreads, 1)
 
 // ------------------------------------------------------------------ 128x128 blocks
 //
-// The 256-row tile holds two blocks; warpgroup h owns block h: each thread its row, the
-// block max through warp shuffles and a 4-warp shared reduction.  Transposed codes are
-// gathered column-wise from the row-code staging box.
-constexpr int QB_STAGES = 2;
+// One 128 x 128 block per tile (two 128 x 64 TMA boxes, 32 KB) in a four-stage ring;
+// warpgroup h (warps 4h .. 4h+3) takes the CTA's tiles h, h+2, ..., so the two warpgroups
+// run independently.  Each thread owns one row of the block; the block max comes from warp
+// shuffles and a 4-warp shared reduction.  Transposed codes are gathered column-wise from
+// the row-code staging box.
+constexpr int QB_STAGES = 4;
+constexpr uint32_t kBlockTile = 2 * kBox;
+template <bool TRANS>
+constexpr size_t block_smem_bytes() { return 1024 + QB_STAGES * kBlockTile + (TRANS ? 4 : 2) * kBox + (2 * QB_STAGES + 2) * 8 + 16 + 32; }
 
 template <bool POW2, bool TRANS>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -392,46 +397,82 @@ __global__ void __launch_bounds__(kQThreads, 1)
                        const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QSmem sm = q_carve<QB_STAGES, TRANS>(smem_raw);
-    q_init<QB_STAGES>(sm);
+    const uint32_t base0 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
+    const uint32_t stage = base0 + pad;
+    const uint32_t out_rows = stage + QB_STAGES * kBlockTile, out_cols = out_rows + 2 * kBox;
+    const uint32_t bars = out_cols + (TRANS ? 2 * kBox : 0);   // full[S], empty[S], warpgroup[2]
+    uint8_t *tail = smem_raw + pad + QB_STAGES * kBlockTile + (TRANS ? 4 : 2) * kBox + (2 * QB_STAGES + 2) * 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail);
+    float *red = reinterpret_cast<float *>(tail + 16);          // 8 per-warp partial maxima
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QB_STAGES; ++i) {
+            mbar_init(bars + 8 * i, 1);
+            mbar_init(bars + 8 * (QB_STAGES + i), 4);             // the four warps of one warpgroup
+        }
+        mbar_init(bars + 8 * (2 * QB_STAGES), 4);
+        mbar_init(bars + 8 * (2 * QB_STAGES + 1), 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
-    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
-    const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
-    if (warp == kConsumers) {
-        if (lane == 0)
-            q_produce<QB_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+    const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;   // rows is a multiple of 128
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    if (warp == kConsumers) {   // producer: one block per tile as two 128 x 64 boxes
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+                const uint32_t st = it % QB_STAGES, ph = (it / QB_STAGES) & 1;
+                if (!mbar_wait(bars + 8 * (QB_STAGES + st), ph ^ 1, ctl, 0x1300 | st))
+                    break;
+                const int64_t rb = item / ncb, cb = item - rb * ncb;
+                mbar_arrive_expect_tx(bars + 8 * st, kBlockTile);
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+                    tma_load_2d(stage + st * kBlockTile + b * kBox, &tmx, bars + 8 * st,
+                                static_cast<int32_t>(cb * 128 + b * 64), static_cast<int32_t>(rb * 128));
+            }
+            for (uint32_t j = it > QB_STAGES ? it - QB_STAGES : 0; j < it; ++j) {   // no load left in flight
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bars + 8 * (j % QB_STAGES), (j / QB_STAGES) & 1))
+                    if (globaltimer_ns() - t0 > p.timeout_ns)
+                        break;
+            }
+        }
         return;
     }
     const int h = t >> 7, rr = t & 127;
-    const uint32_t wgbar = sm.bars + 8 * (2 * QB_STAGES + h);
-    const uint32_t out_r = sm.out_rows + h * kBox, out_c = sm.out_cols + h * kBox;
+    const uint32_t wgbar = bars + 8 * (2 * QB_STAGES + h);
+    const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + h * kBox;
     const bool elected = rr == 0;
-    uint32_t cph = 0, it = 0;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    uint32_t cph = 0;
+    uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
+    for (int64_t item = blockIdx.x + h * static_cast<int64_t>(gridDim.x); item < items;
+         item += 2 * static_cast<int64_t>(gridDim.x), it += 2) {
         const uint32_t st = it % QB_STAGES, ph = (it / QB_STAGES) & 1;
-        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1400 | st))
+        if (!mbar_wait(bars + 8 * st, ph, ctl, 0x1400 | st))
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
-        const int64_t y = rb * kTileRows + h * 128;        // first row of this block
-        const bool block_in = y < p.rows;                   // rows is a multiple of 128
+        const int64_t y = rb * 128;                          // first row of the block
         uint32_t w[64];
-        load_row(sm.stage + st * kTile, t, w);
+        load_row(stage + st * kBlockTile, rr, w);
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(sm.bars + 8 * (QB_STAGES + st));
+            mbar_arrive(bars + 8 * (QB_STAGES + st));
         float a = amax_words(w);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         if (lane == 0)
-            sm.red[warp] = a;
+            red[warp] = a;
         if (elected)
             bulk_wait_read0();                              // the staging boxes are free
         if (!wg_sync(wgbar, cph, ctl, 0x1410))             // block max published
             break;
-        a = fmaxf(fmaxf(sm.red[h * 4], sm.red[h * 4 + 1]), fmaxf(sm.red[h * 4 + 2], sm.red[h * 4 + 3]));
+        a = fmaxf(fmaxf(red[h * 4], red[h * 4 + 1]), fmaxf(red[h * 4 + 2], red[h * 4 + 3]));
         const GroupScale g = make_group_scale(a, POW2);
-        if (rr == 0 && block_in)
+        if (rr == 0)
             p.s[(y / 128) * p.lds + cb] = g.s;
         write_codes(out_r, rr, w, g);
         if (TRANS) {
@@ -454,7 +495,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         fence_proxy_async_smem();
         if (!wg_sync(wgbar, cph, ctl, 0x1412))
             break;
-        if (elected && block_in) {
+        if (elected) {
             tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
             if (TRANS)
                 tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
@@ -696,12 +737,12 @@ cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, co
 cudaError_t launch_quant_block(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
                                const QuantArgs &a, bool pow2, int num_sms, cudaStream_t st)
 {
-    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
+    const int64_t items = (a.rows / 128) * (a.cols / 128);   // rows is a multiple of 128
     if (items == 0)
         return cudaSuccess;
     const bool tr = a.qT != nullptr;
-    constexpr size_t smem_t = q_smem_bytes<QB_STAGES, true>();
-    constexpr size_t smem_n = q_smem_bytes<QB_STAGES, false>();
+    constexpr size_t smem_t = block_smem_bytes<true>();
+    constexpr size_t smem_n = block_smem_bytes<false>();
     if (pow2)
         return tr ? launch_q(quant_block_kernel<true, true>, smem_t, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a)
                   : launch_q(quant_block_kernel<true, false>, smem_n, items, num_sms, st, kQThreads, tmx, tmq, tmqT, a);
