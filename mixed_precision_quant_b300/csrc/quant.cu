@@ -10,17 +10,19 @@
 //   * 128x1 column groups (one scale per column per 128 rows), written transposed,
 //   * 128x128 blocks (one scale per block), optionally also written transposed.
 //
-// Design.  All three kernels are persistent and warp-specialised around tiles of
-// 256 rows x 128 columns of BF16 (64 KB):
-//   * one producer warp loads a tile as four 128-row x 64-column TMA boxes with 128-byte
-//     swizzle into a shared-memory ring (completion counted on mbarriers);
-//   * consumer warps own one row group per thread (rows, blocks: eight warps) or half a
-//     row group and half a column group per thread (dual: sixteen warps, the halves'
-//     max-abs values meeting in one shuffle): a thread reads its values with 16-byte (or,
-//     down a column, 2-byte) shared loads, reduces the max-abs, derives the scale and
-//     converts with the exact arithmetic of quant_device.cuh;
-//   * codes are written into 128-byte-swizzled staging tiles, one per warpgroup, and
-//     leave with TMA bulk-tensor stores (coalesced, clipped at the tensor bounds).
+// Design.  The three BF16 kernels are persistent and warp-specialised around tiles of
+// 128 rows x 128 columns of BF16 (32 KB) in a four-slot ring:
+//   * one producer lane loads a tile as two 128-row x 64-column TMA boxes with 128-byte
+//     swizzle (completion counted on mbarriers);
+//   * the two consumer warpgroups take alternate tiles of the CTA, each with its own
+//     staging tiles and barrier; a thread owns one row group (rows, blocks: eight warps)
+//     or half a row group and half a column group (dual: sixteen warps, the halves'
+//     max-abs values meeting in one shuffle), reads its values with 16-byte (or, down a
+//     column, 2-byte) shared loads, reduces the max-abs, derives the scale and converts
+//     with the exact arithmetic of quant_device.cuh;
+//   * codes are written into 128-byte-swizzled staging tiles and leave with TMA
+//     bulk-tensor stores (coalesced, clipped at the tensor bounds).
+// The re-quantization kernel streams FP8 code tiles the same way (below).
 // Every wait is bounded.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -34,9 +36,7 @@ namespace {
 
 constexpr int kConsumers = 8;                       // consumer warps per CTA
 constexpr int kQThreads = 32 * (kConsumers + 1);    // + one producer warp
-constexpr int kTileRows = 256;                      // rows per tile
 constexpr uint32_t kBox = 128 * 128;                // one 128-row x 128-byte box (16 KB)
-constexpr uint32_t kTile = 4 * kBox;                // 256 x 128 BF16 = 64 KB
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr)
 {
@@ -81,88 +81,15 @@ __device__ __forceinline__ bool wg_sync(uint32_t bar, uint32_t &k, const WaitCtl
     return ok;
 }
 
-// ------------------------------------------------------------------ shared layout
-
-struct QSmem {
-    uint32_t stage;      // ring of BF16 tiles (64 KB each)
-    uint32_t out_rows;   // 2 x 16 KB row-code staging tiles (one per warpgroup)
-    uint32_t out_cols;   // 2 x 16 KB transposed-code staging tiles (one per warpgroup)
-    uint32_t bars;       // full[S], empty[S], wg[2]
-    volatile int *abort;
-    float *red;          // 8 per-warp partial maxima
-};
-
-template <int STAGES, bool COLS>
-constexpr size_t q_smem_bytes() { return 1024 + STAGES * kTile + 2 * kBox + (COLS ? 2 * kBox : 0) + 256; }
-
-template <int STAGES, bool COLS>
-__device__ __forceinline__ QSmem q_carve(uint8_t *raw)
-{
-    QSmem s;
-    const uint32_t base0 = smem_u32(raw);
-    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
-    s.stage = base0 + pad;
-    s.out_rows = s.stage + STAGES * kTile;
-    s.out_cols = s.out_rows + 2 * kBox;
-    s.bars = s.out_cols + (COLS ? 2 * kBox : 0);
-    uint8_t *tail = raw + pad + STAGES * kTile + 2 * kBox + (COLS ? 2 * kBox : 0);
-    s.abort = reinterpret_cast<volatile int *>(tail + (2 * STAGES + 2) * 8);
-    s.red = reinterpret_cast<float *>(tail + (2 * STAGES + 2) * 8 + 16);
-    return s;
-}
-
-template <int STAGES>
-__device__ __forceinline__ void q_init(const QSmem &s)
-{
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(s.bars + 8 * i, 1);
-            mbar_init(s.bars + 8 * (STAGES + i), kConsumers);
-        }
-        mbar_init(s.bars + 8 * (2 * STAGES), 4);
-        mbar_init(s.bars + 8 * (2 * STAGES + 1), 4);
-        *s.abort = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-}
-
-// Producer: one lane streams tile `item` (256-row block rb, 128-column block cb) into the
-// ring as four boxes; out-of-bounds rows read as zero.
-template <int STAGES>
-__device__ __forceinline__ void q_produce(const QSmem &s, const CUtensorMap *tm, int64_t items, int64_t ncb,
-                                          const WaitCtl &ctl, uint64_t timeout_ns)
-{
-    uint32_t it = 0;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
-        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
-        if (!mbar_wait(s.bars + 8 * (STAGES + st), ph ^ 1, ctl, 0x1100 | st))
-            break;
-        const int64_t rb = item / ncb, cb = item - rb * ncb;
-        const uint32_t full = s.bars + 8 * st;
-        mbar_arrive_expect_tx(full, kTile);
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            tma_load_2d(s.stage + st * kTile + b * kBox, tm, full, static_cast<int32_t>(cb * 128 + (b & 1) * 64),
-                        static_cast<int32_t>(rb * kTileRows + (b >> 1) * 128));
-    }
-    for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(s.bars + 8 * (j % STAGES), (j / STAGES) & 1))
-            if (globaltimer_ns() - t0 > timeout_ns)
-                break;
-    }
-}
-
-// Row r (0..255) of the tile at `tile`: its 128 values as 64 BF16x2 words, memory order.
+// Row r (0..127) of the 128 x 128 BF16 tile at `tile` (two 128 x 64 boxes): its 128 values
+// as 64 BF16x2 words, memory order.
 __device__ __forceinline__ void load_row(uint32_t tile, int r, uint32_t (&w)[64])
 {
-    const int rh = r >> 7, rr = r & 127;
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint4 v = lds_v4(tile + (rh * 2 + ch) * kBox + sw128(rr, j));
+            const uint4 v = lds_v4(tile + ch * kBox + sw128(r, j));
             w[ch * 32 + j * 4 + 0] = v.x;
             w[ch * 32 + j * 4 + 1] = v.y;
             w[ch * 32 + j * 4 + 2] = v.z;
@@ -178,11 +105,40 @@ __device__ __forceinline__ void write_codes(uint32_t box, int r, const uint32_t 
         sts_v4(box + sw128(r, q), codes16(&w[q * 8], g));
 }
 
+// Producer of the 128-row kernels: one lane streams tile `item` (128-row block rb, 128-column
+// block cb) into a ring of `stages` 32 KB slots as two 128 x 64 boxes (rows past the tensor
+// read as zero), then waits (bounded) until its last loads have landed.
+__device__ __forceinline__ void produce128(uint32_t stage, uint32_t bars, int stages, const CUtensorMap *tm,
+                                           int64_t items, int64_t ncb, const WaitCtl &ctl, uint64_t timeout_ns,
+                                           int tag)
+{
+    uint32_t it = 0;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+        const uint32_t st = it % stages, ph = (it / stages) & 1;
+        if (!mbar_wait(bars + 8 * (stages + st), ph ^ 1, ctl, tag | st))
+            break;
+        const int64_t rb = item / ncb, cb = item - rb * ncb;
+        mbar_arrive_expect_tx(bars + 8 * st, 2 * kBox);
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            tma_load_2d(stage + st * 2 * kBox + b * kBox, tm, bars + 8 * st, static_cast<int32_t>(cb * 128 + b * 64),
+                        static_cast<int32_t>(rb * 128));
+    }
+    for (uint32_t j = it > static_cast<uint32_t>(stages) ? it - stages : 0; j < it; ++j) {   // no load in flight
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bars + 8 * (j % stages), (j / stages) & 1))
+            if (globaltimer_ns() - t0 > timeout_ns)
+                break;
+    }
+}
+
 // ------------------------------------------------------------------ 1x128 rows
 //
-// Thread t of the consumers owns row t of the tile; warpgroup h (threads 128h .. +127)
-// owns rows 128h .. +127 and their staging box.
-constexpr int QR_STAGES = 2;
+// One 128-row x 128-column tile per ring slot (four slots); warpgroup h (threads
+// 128h .. +127) takes the CTA's tiles h, h+2, ..., thread rr owning row rr of the tile, with
+// its own staging box and barrier, so the two warpgroups run independently.
+constexpr int QR_STAGES = 4;
+constexpr size_t kRowsSmem = 1024 + QR_STAGES * 2 * kBox + 2 * kBox + (2 * QR_STAGES + 2) * 8 + 16;
 
 template <bool POW2>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -190,33 +146,50 @@ __global__ void __launch_bounds__(kQThreads, 1)
                       const QuantArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
-    const QSmem sm = q_carve<QR_STAGES, false>(smem_raw);
-    q_init<QR_STAGES>(sm);
+    const uint32_t base0 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
+    const uint32_t stage = base0 + pad, out_rows = stage + QR_STAGES * 2 * kBox;
+    const uint32_t bars = out_rows + 2 * kBox;          // full[S], empty[S], warpgroup[2]
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(smem_raw + pad + QR_STAGES * 2 * kBox + 2 * kBox + (2 * QR_STAGES + 2) * 8);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QR_STAGES; ++i) {
+            mbar_init(bars + 8 * i, 1);
+            mbar_init(bars + 8 * (QR_STAGES + i), 4);  // the four warps of one warpgroup
+        }
+        mbar_init(bars + 8 * (2 * QR_STAGES), 4);
+        mbar_init(bars + 8 * (2 * QR_STAGES + 1), 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
-    const int64_t ncb = p.cols / 128, items = ((p.rows + kTileRows - 1) / kTileRows) * ncb;
-    const WaitCtl ctl{sm.abort, p.status, p.timeout_ns};
+    const int64_t ncb = p.cols / 128, items = ((p.rows + 127) / 128) * ncb;
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     if (warp == kConsumers) {
         if (lane == 0)
-            q_produce<QR_STAGES>(sm, &tmx, items, ncb, ctl, p.timeout_ns);
+            produce128(stage, bars, QR_STAGES, &tmx, items, ncb, ctl, p.timeout_ns, 0x1100);
         return;
     }
     const int h = t >> 7, rr = t & 127;
-    const uint32_t wgbar = sm.bars + 8 * (2 * QR_STAGES + h);
-    const uint32_t out = sm.out_rows + h * kBox;
+    const uint32_t wgbar = bars + 8 * (2 * QR_STAGES + h);
+    const uint32_t out = out_rows + h * kBox;
     const bool elected = rr == 0;
-    uint32_t cph = 0, it = 0;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+    uint32_t cph = 0;
+    uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
+    for (int64_t item = blockIdx.x + h * static_cast<int64_t>(gridDim.x); item < items;
+         item += 2 * static_cast<int64_t>(gridDim.x), it += 2) {
         const uint32_t st = it % QR_STAGES, ph = (it / QR_STAGES) & 1;
-        if (!mbar_wait(sm.bars + 8 * st, ph, ctl, 0x1200 | st))
+        if (!mbar_wait(bars + 8 * st, ph, ctl, 0x1200 | st))
             break;
         const int64_t rb = item / ncb, kb = item - rb * ncb;
         uint32_t w[64];
-        load_row(sm.stage + st * kTile, t, w);
+        load_row(stage + st * 2 * kBox, rr, w);
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(sm.bars + 8 * (QR_STAGES + st));
+            mbar_arrive(bars + 8 * (QR_STAGES + st));
         const GroupScale g = make_group_scale(amax_words(w), POW2);
-        const int64_t r = rb * kTileRows + t;
+        const int64_t r = rb * 128 + rr;
         if (r < p.rows)
             p.s[kb * p.lds + r] = g.s;
         if (elected)
@@ -227,9 +200,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         fence_proxy_async_smem();
         if (!wg_sync(wgbar, cph, ctl, 0x1211))
             break;
-        const int64_t y = rb * kTileRows + h * 128;
-        if (elected && y < p.rows) {
-            tma_store_2d(&tmq, out, static_cast<int32_t>(kb * 128), static_cast<int32_t>(y));
+        if (elected) {
+            tma_store_2d(&tmq, out, static_cast<int32_t>(kb * 128), static_cast<int32_t>(rb * 128));
             bulk_commit();
         }
     }
@@ -284,26 +256,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;   // rows is a multiple of 128
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     if (warp == kDualConsumers) {   // producer: one 128-row tile as two 128 x 64 boxes
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
-                const uint32_t st = it % QD_STAGES, ph = (it / QD_STAGES) & 1;
-                if (!mbar_wait(bars + 8 * (QD_STAGES + st), ph ^ 1, ctl, 0x1400 | st))
-                    break;
-                const int64_t rb = item / ncb, cb = item - rb * ncb;
-                mbar_arrive_expect_tx(bars + 8 * st, kDualTile);
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
-                    tma_load_2d(stage + st * kDualTile + b * kBox, &tmx, bars + 8 * st,
-                                static_cast<int32_t>(cb * 128 + b * 64), static_cast<int32_t>(rb * 128));
-            }
-            for (uint32_t j = it > QD_STAGES ? it - QD_STAGES : 0; j < it; ++j) {   // no load left in flight
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(bars + 8 * (j % QD_STAGES), (j / QD_STAGES) & 1))
-                    if (globaltimer_ns() - t0 > p.timeout_ns)
-                        break;
-            }
-        }
+        if (lane == 0)
+            produce128(stage, bars, QD_STAGES, &tmx, items, ncb, ctl, p.timeout_ns, 0x1400);
         return;
     }
     const int h = t >> 8, u = t & 255;
@@ -420,26 +374,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int64_t ncb = p.cols / 128, items = (p.rows / 128) * ncb;   // rows is a multiple of 128
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     if (warp == kConsumers) {   // producer: one block per tile as two 128 x 64 boxes
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
-                const uint32_t st = it % QB_STAGES, ph = (it / QB_STAGES) & 1;
-                if (!mbar_wait(bars + 8 * (QB_STAGES + st), ph ^ 1, ctl, 0x1300 | st))
-                    break;
-                const int64_t rb = item / ncb, cb = item - rb * ncb;
-                mbar_arrive_expect_tx(bars + 8 * st, kBlockTile);
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
-                    tma_load_2d(stage + st * kBlockTile + b * kBox, &tmx, bars + 8 * st,
-                                static_cast<int32_t>(cb * 128 + b * 64), static_cast<int32_t>(rb * 128));
-            }
-            for (uint32_t j = it > QB_STAGES ? it - QB_STAGES : 0; j < it; ++j) {   // no load left in flight
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(bars + 8 * (j % QB_STAGES), (j / QB_STAGES) & 1))
-                    if (globaltimer_ns() - t0 > p.timeout_ns)
-                        break;
-            }
-        }
+        if (lane == 0)
+            produce128(stage, bars, QB_STAGES, &tmx, items, ncb, ctl, p.timeout_ns, 0x1300);
         return;
     }
     const int h = t >> 7, rr = t & 127;
@@ -707,10 +643,10 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
 cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, const QuantArgs &a, bool pow2,
                               int num_sms, cudaStream_t st)
 {
-    const int64_t items = ((a.rows + kTileRows - 1) / kTileRows) * (a.cols / 128);
+    const int64_t items = ((a.rows + 127) / 128) * (a.cols / 128);
     if (items == 0)
         return cudaSuccess;
-    constexpr size_t smem = q_smem_bytes<QR_STAGES, false>();
+    constexpr size_t smem = kRowsSmem;
     return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, kQThreads, tmx, tmq, a)
                 : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, kQThreads, tmx, tmq, a);
 }
