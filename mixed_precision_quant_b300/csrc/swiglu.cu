@@ -26,7 +26,7 @@
 namespace mpq {
 namespace {
 
-constexpr int kSwThreads = 256;
+constexpr int kSwThreads = 128;
 constexpr int kSwLpg = 4;                  // lanes per group
 constexpr int kSwCpl = 16 / kSwLpg;        // 16-byte chunks per lane, per half
 constexpr int kSwU = 1;                    // groups per lane and batch
