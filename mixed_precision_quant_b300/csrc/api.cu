@@ -99,10 +99,11 @@ mpq_status encode_codes(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, i
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
 
-// GEMM output view [rows, cols] (cols contiguous, BF16 or FP32), box 64 bytes x 32 rows,
-// 64-byte swizzle (the layout of the kernel's staging buffers); stores are clipped at the
-// tensor bounds.
-mpq_status encode_output(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32)
+// GEMM output view [rows, cols] (cols contiguous, BF16 or FP32), boxes of 32 rows x 128
+// bytes with 128-byte swizzle (wide: the pair kernel's staging buffers) or 32 rows x 64
+// bytes with 64-byte swizzle (the single-SM kernel's); stores are clipped at the tensor
+// bounds.
+mpq_status encode_output(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32, bool wide)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
@@ -110,10 +111,10 @@ mpq_status encode_output(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, 
     const int64_t esz = fp32 ? 4 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esz)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>((wide ? 128 : 64) / esz), 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MPQ_OK : MPQ_ERR_CUDA;
 }
@@ -451,7 +452,7 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     if ((st = encode_operand(&tmB, B, N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
         return st;
     CUtensorMap tmC;
-    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
+    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32, pair)) != MPQ_OK)
         return st;
     mpq::GemmArgs a{};
     a.M = M; a.N = N; a.K = K;
@@ -521,7 +522,7 @@ static mpq_status launch_fused_grouped(mpq_handle h, void *workspace, int64_t G,
         return e;
     if ((e = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(false))) != MPQ_OK)
         return e;
-    if ((e = encode_output(&tmC, C, M_total, N, ldc, fp32)) != MPQ_OK)
+    if ((e = encode_output(&tmC, C, M_total, N, ldc, fp32, false)) != MPQ_OK)
         return e;
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, fp32, false, h->num_sms, st, &f));
 }
@@ -646,7 +647,7 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
         return st;
     CUtensorMap tmC;
-    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32)) != MPQ_OK)
+    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32, pair)) != MPQ_OK)
         return st;
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, pair,
                                       h->num_sms,

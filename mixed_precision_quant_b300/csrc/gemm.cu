@@ -30,9 +30,9 @@
 //   warps 4-11  promotion: tcgen05.ld the slice partial (two loads in flight), multiply
 //               by its two scales and accumulate into FP32 registers with scalar FMAs;
 //               promotion of slice k overlaps the MMAs of slice k+1.  The finished tile is
-//               written as BF16 or FP32 through swizzled staging buffers (four of 2 KB per
+//               written as BF16 or FP32 through swizzled staging buffers (two of 4 KB per
 //               warp in pair mode, so the stores drain while the next tile starts) and TMA
-//               bulk-tensor stores (32 rows x 64 bytes per store).
+//               bulk-tensor stores (32 rows x 128 bytes per store; 64 bytes single-SM).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
@@ -45,7 +45,6 @@ namespace {
 constexpr int BK = 128;              // K per promotion slice
 constexpr int BN = 256;              // output columns per tile
 constexpr int SSLOTS = 4;            // scale ring depth (slices)
-constexpr uint32_t STAGE_OUT = 2048; // one output staging buffer (32 rows x 64 B)
 constexpr int kThreads = 384;
 constexpr uint32_t A_BYTES = 128 * BK;     // 128 rows of A per CTA per slice
 constexpr uint32_t TMEM_COLS = 512;        // two 256-column partial buffers
@@ -54,10 +53,15 @@ constexpr int kMaxGroups = 1024;
 template <bool PAIR>
 struct Cfg {
     static constexpr int STAGES = 4;
-    // Staging buffers per promotion warp: in pair mode four (8 KB, a whole warp tile in BF16),
-    // so a tile's TMA stores drain during the next tile's main loop instead of holding the
-    // warp back -- the output is written in a burst, when the write path is saturated.
-    static constexpr int OUT_BUFS = PAIR ? 4 : 1;
+    // Output staging per promotion warp: in pair mode two 4 KB buffers of 32 rows x 128 bytes
+    // (8 KB, a whole warp tile in BF16), so a tile's TMA stores drain during the next tile's
+    // main loop instead of holding the warp back -- the output is written in a burst, when
+    // the write path is saturated.  128-byte rows halve the number of row pieces the TMA
+    // unit writes against 64-byte rows (Dgrad 8192 x 7168 x 2048 +4%, Fprop +1%).  The
+    // single-SM form has no room for more than one 2 KB buffer of 64-byte rows.
+    static constexpr int OUT_BUFS = PAIR ? 2 : 1;
+    static constexpr uint32_t STAGE_OUT = PAIR ? 4096 : 2048;
+    static constexpr int ROWB = STAGE_OUT / 32;              // bytes per staged row piece
     static constexpr int B_ROWS = PAIR ? 128 : 256;          // B rows staged by one CTA per slice
     static constexpr uint32_t B_BYTES = B_ROWS * BK;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *smA = base;
     uint8_t *smB = smA + STAGES * A_BYTES;
-    uint8_t *smO = smB + STAGES * C::B_BYTES;                    // output staging, 8 x OUT_BUFS x 2 KB
-    float *ssa = reinterpret_cast<float *>(smO + 8 * C::OUT_BUFS * STAGE_OUT);
+    uint8_t *smO = smB + STAGES * C::B_BYTES;                    // output staging, 8 x OUT_BUFS x STAGE_OUT
+    float *ssa = reinterpret_cast<float *>(smO + 8 * C::OUT_BUFS * C::STAGE_OUT);
     float *ssb = ssa + SSLOTS * 128;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ssb + SSLOTS * BN);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBARS);
@@ -569,27 +573,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ncol0 < N) {
                 const bool whole = GROUPED ? (wrow0 + 32 <= ti.row_end) : true;
                 if (whole) {
-                    const uint32_t stg0 = smem_u32(smO + ew * C::OUT_BUFS * STAGE_OUT);
-                    constexpr int COLS = OUT_F32 ? 16 : 32;          // columns per 64-byte row piece
+                    const uint32_t stg0 = smem_u32(smO + ew * C::OUT_BUFS * C::STAGE_OUT);
+                    constexpr int COLS = C::ROWB / (OUT_F32 ? 4 : 2);   // columns per row piece
+                    constexpr int PCS = C::ROWB / 16;                   // 16-byte pieces per row piece
 #pragma unroll
                     for (int ch = 0; ch < 128 / COLS; ++ch) {
-                        const uint32_t stg_u32 = stg0 + (ch % C::OUT_BUFS) * STAGE_OUT;
+                        const uint32_t stg_u32 = stg0 + (ch % C::OUT_BUFS) * C::STAGE_OUT;
                         if (lane == 0) {                                // the buffer's last piece has left smem
                             if (C::OUT_BUFS == 4)
                                 bulk_wait_read3();
+                            else if (C::OUT_BUFS == 2)
+                                bulk_wait_read1();
                             else
                                 bulk_wait_read0();
                         }
                         __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {                   // four 16-byte pieces of the row
+                        for (int j = 0; j < PCS; ++j) {                 // 16-byte pieces of the row
                             uint4 w;
                             if (OUT_F32) {
-                                const int a0 = ch * 16 + j * 4;         // columns ch*16+4j..+3
+                                const int a0 = ch * COLS + j * 4;         // columns ch*16+4j..+3
                                 w = make_uint4(__float_as_uint(acc[a0]), __float_as_uint(acc[a0 + 1]),
                                                __float_as_uint(acc[a0 + 2]), __float_as_uint(acc[a0 + 3]));
                             } else {
-                                const int a0 = ch * 32 + j * 8;         // columns ch*32+8j..+7
+                                const int a0 = ch * COLS + j * 8;         // columns ch*32+8j..+7
                                 uint32_t h[4];
 #pragma unroll
                                 for (int k = 0; k < 4; ++k) {
@@ -598,8 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                                 w = make_uint4(h[0], h[1], h[2], h[3]);
                             }
-                            // 64-byte swizzle: 16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3)
-                            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+                            // 128-byte swizzle: 16-byte piece j of row r sits at piece j ^ (r & 7);
+                            // 64-byte swizzle: at piece j ^ ((r >> 1) & 3)
+                            const uint32_t off = PCS == 8 ? lane * 128 + ((j ^ (lane & 7)) << 4)
+                                                          : lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
                             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg_u32 + off), "r"(w.x),
                                          "r"(w.y), "r"(w.z), "r"(w.w)
                                          : "memory");
