@@ -18,7 +18,7 @@
 //     staging tiles and barrier; a thread owns one row group (rows, blocks: eight warps)
 //     or half a row group and half a column group (dual: sixteen warps, the halves'
 //     max-abs values meeting in one shuffle), reads its values with 16-byte (or, down a
-//     column, 2-byte) shared loads, reduces the max-abs, derives the scale and converts
+//     column, transposing 8x8 matrix) shared loads, reduces the max-abs, derives the scale and converts
 //     with the exact arithmetic of quant_device.cuh;
 //   * codes are written into 128-byte-swizzled staging tiles and leave with TMA
 //     bulk-tensor stores (coalesced, clipped at the tensor bounds).
@@ -57,6 +57,21 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t addr)
     uint16_t v;
     asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+
+// Four 8x8 matrices of 16-bit values, transposed on the way in: lane L names row L % 8 of
+// matrix L / 8 (16 bytes); lane t receives in v[m] the two values of column t / 4 of
+// matrix m at rows 2 (t % 4) (low half) and 2 (t % 4) + 1 (high half).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t *v)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(addr));
 }
 
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v)
@@ -220,8 +235,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // BF16, two 128 x 64 TMA boxes) in a four-stage ring; warpgroup h (warps 8h .. 8h+7) takes
 // the CTA's tiles h, h+2, h+4, ..., so the two warpgroups run independently, each with its
 // own staging tiles and barrier.  Within a warpgroup thread u (0..255) holds
-//   row pass:    row u/2, columns 64 (u%2) .. +63;
-//   column pass: column u/2, rows 64 (u%2) .. +63.
+//   row pass:    row u/2, columns 64 (u%2) .. +63 (16-byte shared loads);
+//   column pass: lane t of warp wl, for the two columns 16 wl + 8 b + t/4 (b = 0, 1), the
+//                rows 8 rb + 2 (t%4), +1 (rb = 0..15) -- transposing 8x8 matrix loads
+//                (ldmatrix .trans) deliver each as one BF16 pair, 128 bytes per shared
+//                wavefront, so the four lanes of a column hold its 128 values and combine
+//                max-abs values in two shuffles; codes leave as 2-byte shared stores.
 constexpr int QD_STAGES = 4;
 constexpr uint32_t kDualTile = 2 * kBox;          // 128 x 128 BF16
 constexpr int kDualConsumers = 16;
@@ -261,7 +280,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         return;
     }
     const int h = t >> 8, u = t & 255;
-    const int g2 = u >> 1, sub = u & 1;                    // group (row or column) and half
+    const int g2 = u >> 1, sub = u & 1;                    // row pass: row and half
+    const int wl = u >> 5;                                  // warp within the warpgroup
     const uint32_t wgbar = bars + 8 * (2 * QD_STAGES + h);
     const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + h * kBox;
     const bool elected = u == 0;
@@ -279,8 +299,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             bulk_wait_read0();                             // both staging boxes are free
         if (!wg_sync(wgbar, cph, ctl, 0x1510))
             break;
-        uint32_t w[32];
         if (ROWS) {
+            uint32_t w[32];
             const uint32_t box = tile + sub * kBox;          // columns 64 sub .. +63
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -296,28 +316,42 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             for (int q = 0; q < 4; ++q)
                 sts_v4(out_r + sw128(g2, sub * 4 + q), codes16(&w[q * 8], g));
         }
-        {
-            const uint32_t box = tile + (g2 >> 6) * kBox;
-            const int j = (g2 & 63) >> 3, e = (g2 & 7) << 1;
+        // Column pass: warp wl of the warpgroup owns columns 16 wl .. +15 as two 8-column
+        // blocks; transposing 8x8 loads give lane t, for column 16 wl + 8 b + t / 4, the BF16
+        // pair of rows 8 rb + 2 (t % 4), +1 in wc[b][rb] (rb = 0..15), so the four lanes
+        // t / 4 = const hold the column's 128 values and meet in two shuffles.
+        uint32_t wc[2][16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t lo = lds_u16(box + sw128(64 * sub + 2 * i, j) + e);
-                const uint32_t hi = lds_u16(box + sw128(64 * sub + 2 * i + 1, j) + e);
-                w[i] = lo | (hi << 16);
-            }
+        for (int b = 0; b < 2; ++b) {
+            const int cbk = 2 * wl + b;                      // 8-column block, 0..15
+            const uint32_t box = tile + (cbk >> 3) * kBox;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)                      // row blocks 4i .. 4i+3: rows 32i + lane
+                ldsm_x4_trans(box + sw128(32 * i + lane, cbk & 7), &wc[b][4 * i]);
+        }
+        float ac[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            ac[b] = amax_words(wc[b]);
+            ac[b] = fmaxf(ac[b], __shfl_xor_sync(0xffffffffu, ac[b], 1));
+            ac[b] = fmaxf(ac[b], __shfl_xor_sync(0xffffffffu, ac[b], 2));
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(bars + 8 * (QD_STAGES + st));      // this warp has read the tile
-        {
-            float a = amax_words(w);
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            const GroupScale g = make_group_scale(a, POW2);
-            if (sub == 0)
-                p.sT[(y / 128) * p.ldsT + cb * 128 + g2] = g.s;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                sts_v4(out_c + sw128(g2, sub * 4 + q), codes16(&w[q * 8], g));
+        for (int b = 0; b < 2; ++b) {
+            const int c = 16 * wl + 8 * b + (lane >> 2), k2 = (lane & 3) * 2;
+            const GroupScale g = make_group_scale(ac[b], POW2);
+            if (k2 == 0)
+                p.sT[(y / 128) * p.ldsT + cb * 128 + c] = g.s;
+            uint32_t o[8];                                   // o[j]: rows 16j + k2, +1 | 16j + 8 + k2, +1
+            codes_words<16>(wc[b], g, o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                sts_u16(out_c + sw128(c, j) + k2, o[j]);
+                sts_u16(out_c + sw128(c, j) + 8 + k2, o[j] >> 16);
+            }
         }
         fence_proxy_async_smem();
         if (!wg_sync(wgbar, cph, ctl, 0x1511))
