@@ -565,8 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Output: rows [ti.row0 + 32 quad, +32), columns [ti.n0 + 128 half, +128).  A warp
-            // whose 32 rows all belong to this tile stages 64-byte row pieces in its swizzled
-            // 2 KB buffer and writes them with TMA stores (clipped at the tensor bounds);
+            // whose 32 rows all belong to this tile stages row pieces (128 bytes in pair mode,
+            // 64 single-SM) in its swizzled buffers and writes them with TMA stores (clipped at
+            // the tensor bounds);
             // a warp on a ragged expert boundary stores its valid rows directly.
             const int wrow0 = ti.row0 + quad * 32;
             const int ncol0 = ti.n0 + half * 128;
