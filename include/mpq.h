@@ -27,7 +27,8 @@
  *   - BF16 inputs are passed as `const void *` (16-bit bfloat16 elements).
  *   - E4M3 codes are bytes; scales are float32.
  *   - `stream` is a cudaStream_t (passed as void *); every call only enqueues work on
- *     it and returns without synchronizing.  The caller's device must be current.
+ *     it and returns without synchronizing.  The device the handle was created on must be
+ *     current (else MPQ_ERR_DEVICE, before any launch).
  *   - Arguments are validated on the host before anything is launched; a validation
  *     failure returns a status code and leaves all outputs untouched.
  *   - Device-side waits are bounded (about one second by default).  A wait that runs
@@ -52,7 +53,9 @@ typedef enum mpq_status {
     MPQ_ERR_UNSUPPORTED = 4, /* unknown op, dtype or flag combination                     */
     MPQ_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed                       */
     MPQ_ERR_TIMEOUT = 6,     /* a device-side wait ran out (reported by the status word)  */
-    MPQ_ERR_WORKSPACE = 7    /* no workspace set on the handle, or it is too small        */
+    MPQ_ERR_WORKSPACE = 7,   /* no workspace set on the handle, or it is too small        */
+    MPQ_ERR_DEVICE = 8       /* the current CUDA device is not the one the handle was
+                                created on (nothing was launched)                         */
 } mpq_status;
 
 typedef enum mpq_op {
@@ -88,7 +91,8 @@ const char *mpq_status_string(int status);
  * share its handover area and must not run concurrently (issue them on one stream). */
 mpq_status mpq_create(mpq_handle *out);
 
-/* Destroy a handle and free its device memory.  Synchronizes the device first. */
+/* Destroy a handle and free its device memory.  Synchronizes the handle's device first
+ * (making it current for the call, then restoring the caller's current device). */
 mpq_status mpq_destroy(mpq_handle h);
 
 /* Limit for every device-side wait launched through this handle, in nanoseconds

@@ -28,7 +28,8 @@ FUSE_QUANT_A = 8
 
 _STATUS = {0: "ok", 1: "null pointer argument", 2: "invalid size or leading dimension",
            3: "misaligned pointer or stride", 4: "unsupported op, dtype or flags",
-           5: "CUDA call failed", 6: "device-side wait timed out", 7: "no workspace set, or too small"}
+           5: "CUDA call failed", 6: "device-side wait timed out", 7: "no workspace set, or too small",
+           8: "the current device is not the handle's device"}
 
 
 class MPQError(RuntimeError):
@@ -145,9 +146,10 @@ def fp8_quant_tile_1x128(x: torch.Tensor, *, pow2: bool = False, rows_out: bool 
         sT = sT if sT is not None else torch.empty((rows // 128, cols), dtype=torch.float32, device=dev)
     else:
         qT = sT = None
-    st = _lib.fp8_quant_tile_1x128(_handle(dev), _ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q), _ptr(s), _ld(s),
-                                   _ptr(qT), _ld(qT), _ptr(sT), _ld(sT), POW2 if pow2 else 0,
-                                   _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_quant_tile_1x128(_handle(dev), _ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q), _ptr(s), _ld(s),
+                                       _ptr(qT), _ld(qT), _ptr(sT), _ld(sT), POW2 if pow2 else 0,
+                                       _stream(dev, stream))
     _check("fp8_quant_tile_1x128", st)
     return q, s, qT, sT
 
@@ -163,8 +165,9 @@ def fp8_swiglu_quant_1x128(hcat: torch.Tensor, *, pow2: bool = True, q=None, s=N
     dev = hcat.device
     q = q if q is not None else torch.empty((rows, width), dtype=torch.uint8, device=dev)
     s = s if s is not None else torch.empty((width // 128, rows), dtype=torch.float32, device=dev)
-    st = _lib.fp8_swiglu_quant_1x128(_handle(dev), _ptr(hcat), rows, width, _ld(hcat), _ptr(q), _ld(q), _ptr(s),
-                                     _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_swiglu_quant_1x128(_handle(dev), _ptr(hcat), rows, width, _ld(hcat), _ptr(q), _ld(q), _ptr(s),
+                                         _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
     _check("fp8_swiglu_quant_1x128", st)
     return q, s
 
@@ -182,8 +185,9 @@ def fp8_requant_tile_128x1(q: torch.Tensor, s: torch.Tensor, *, pow2: bool = Fal
     dev = q.device
     qT = qT if qT is not None else torch.empty((cols, rows), dtype=torch.uint8, device=dev)
     sT = sT if sT is not None else torch.empty((rows // 128, cols), dtype=torch.float32, device=dev)
-    st = _lib.fp8_requant_tile_128x1(_handle(dev), _ptr(q), rows, cols, _ld(q), _ptr(s), _ld(s), _ptr(qT), _ld(qT),
-                                     _ptr(sT), _ld(sT), POW2 if pow2 else 0, _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_requant_tile_128x1(_handle(dev), _ptr(q), rows, cols, _ld(q), _ptr(s), _ld(s), _ptr(qT), _ld(qT),
+                                         _ptr(sT), _ld(sT), POW2 if pow2 else 0, _stream(dev, stream))
     _check("fp8_requant_tile_128x1", st)
     return qT, sT
 
@@ -202,8 +206,9 @@ def fp8_quant_block_128x128(w: torch.Tensor, *, pow2: bool = False, transposed: 
     else:
         qT = None
     s = s if s is not None else torch.empty((rows // 128, cols // 128), dtype=torch.float32, device=dev)
-    st = _lib.fp8_quant_block_128x128(_handle(dev), _ptr(w), rows, cols, _ld(w), _ptr(q), _ld(q), _ptr(qT),
-                                      _ld(qT), _ptr(s), _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_quant_block_128x128(_handle(dev), _ptr(w), rows, cols, _ld(w), _ptr(q), _ld(q), _ptr(qT),
+                                          _ld(qT), _ptr(s), _ld(s), POW2 if pow2 else 0, _stream(dev, stream))
     _check("fp8_quant_block_128x128", st)
     return q, qT, s
 
@@ -231,9 +236,10 @@ def fp8_gemm_blockscaled(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Te
         raise ValueError("A and B disagree on K")
     dev = A.device
     C = _out(M, N, out_dtype, C, dev)
-    st = _lib.fp8_gemm_blockscaled(_handle(dev), int(op), M, N, K, _ptr(A), _ld(A), _ptr(sA), _ld(sA), _ptr(B),
-                                   _ld(B), _ptr(sB), _ld(sB), _ptr(C), _ld(C), int(out_dtype),
-                                   _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_gemm_blockscaled(_handle(dev), int(op), M, N, K, _ptr(A), _ld(A), _ptr(sA), _ld(sA), _ptr(B),
+                                       _ld(B), _ptr(sB), _ld(sB), _ptr(C), _ld(C), int(out_dtype),
+                                       _stream(dev, stream))
     _check("fp8_gemm_blockscaled", st)
     return C
 
@@ -296,9 +302,10 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
     C = _out(M, N, out_dtype, C, dev)
     if fuse_quant:
         _ensure_workspace(dev, fused_workspace_bytes(M, K, G))
-    st = _lib.fp8_grouped_gemm_blockscaled(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(A), _ld(A), _ptr(sA),
-                                           _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
-                                           int(out_dtype), flags, _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_grouped_gemm_blockscaled(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(A), _ld(A), _ptr(sA),
+                                               _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C),
+                                               int(out_dtype), flags, _stream(dev, stream))
     _check("fp8_grouped_gemm_blockscaled", st)
     return C
 
@@ -324,9 +331,10 @@ def fp8_grouped_gemm_fused_quant_noalloc(offsets: torch.Tensor, X: torch.Tensor,
     if offsets.numel() != G + 1 or X.shape[1] != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch between offsets, X, B and C")
     dev = X.device
-    st = _lib.fp8_grouped_gemm_fused_quant_noalloc(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(X), _ld(X), _ptr(B),
-                                                   K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C), int(out_dtype),
-                                                   POW2 if pow2 else 0, _stream(dev, stream))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_grouped_gemm_fused_quant_noalloc(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(X), _ld(X), _ptr(B),
+                                                       K, _ptr(sB), sB.shape[2], _ptr(C), _ld(C), int(out_dtype),
+                                                       POW2 if pow2 else 0, _stream(dev, stream))
     _check("fp8_grouped_gemm_fused_quant_noalloc", st)
     return C
 
@@ -337,7 +345,8 @@ def mpq_check_device_status(device=None, stream=None):
     """Synchronize the stream and return (status, where) from the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     where = ctypes.c_int(0)
-    st = _lib.mpq_check_device_status(_handle(dev), _stream(dev, stream), ctypes.byref(where))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.mpq_check_device_status(_handle(dev), _stream(dev, stream), ctypes.byref(where))
     return st, where.value
 
 
@@ -364,5 +373,6 @@ def mpq_set_gemm_stream_k(mode, device=None):
 
 def mpq_selftest_wait_timeout(timeout_ns: int = 1_000_000, device=None, stream=None):
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    _check("mpq_selftest_wait_timeout", _lib.mpq_selftest_wait_timeout(_handle(dev), int(timeout_ns),
-                                                                         _stream(dev, stream)))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        _check("mpq_selftest_wait_timeout", _lib.mpq_selftest_wait_timeout(_handle(dev), int(timeout_ns),
+                                                                             _stream(dev, stream)))

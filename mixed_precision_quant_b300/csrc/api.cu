@@ -121,6 +121,17 @@ mpq_status encode_output(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, 
 
 mpq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPQ_OK : MPQ_ERR_CUDA; }
 
+// Every buffer of a handle lives on the device that was current at mpq_create, and the
+// kernels launch on the current device: a call made with another device current returns
+// MPQ_ERR_DEVICE before anything is launched.
+mpq_status device_ok(mpq_handle h)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MPQ_ERR_CUDA;
+    return dev == h->device ? MPQ_OK : MPQ_ERR_DEVICE;
+}
+
 } // namespace
 
 extern "C" {
@@ -138,6 +149,7 @@ const char *mpq_status_string(int s)
     case MPQ_ERR_CUDA: return "CUDA call failed";
     case MPQ_ERR_TIMEOUT: return "device-side wait timed out";
     case MPQ_ERR_WORKSPACE: return "no workspace set, or too small";
+    case MPQ_ERR_DEVICE: return "the current device is not the handle's device";
     default: return "unknown status";
     }
 }
@@ -185,10 +197,16 @@ mpq_status mpq_destroy(mpq_handle h)
 {
     if (h == nullptr)
         return MPQ_ERR_NULL;
+    // Synchronize and free on the handle's device, then restore the caller's current device.
+    int cur = -1;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != h->device &&
+                          cudaSetDevice(h->device) == cudaSuccess;
     cudaDeviceSynchronize();
     cudaError_t e = cudaFree(h->d_status);
     const cudaError_t e2 = cudaFree(h->d_sk_flags);
     const cudaError_t e3 = cudaFree(h->d_sk_part);
+    if (switched)
+        cudaSetDevice(cur);
     delete h;
     return from_cuda(e != cudaSuccess ? e : e2 != cudaSuccess ? e2 : e3);
 }
@@ -289,6 +307,8 @@ mpq_status fp8_quant_tile_1x128(mpq_handle h, const void *x, int64_t rows, int64
         return MPQ_OK;
     if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
         return MPQ_ERR_SHAPE;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     const bool pow2 = (flags & MPQ_POW2) != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     mpq::QuantArgs a{};
@@ -328,6 +348,8 @@ mpq_status fp8_swiglu_quant_1x128(mpq_handle h, const void *hcat, int64_t rows, 
         return MPQ_ERR_ALIGN;
     if (rows > (int64_t(1) << 31) || width > (int64_t(1) << 30))
         return MPQ_ERR_SHAPE;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     mpq::SwigluArgs a{};
     a.h = static_cast<const uint16_t *>(hcat);
     a.rows = rows; a.width = width; a.ldh = ldh;
@@ -356,6 +378,8 @@ mpq_status fp8_requant_tile_128x1(mpq_handle h, const uint8_t *q, int64_t rows, 
         return MPQ_ERR_ALIGN;
     if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
         return MPQ_ERR_SHAPE;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     mpq::RequantArgs a{};
     a.rows = rows; a.cols = cols;
     a.s = s; a.lds = lds; a.sT = sT; a.ldsT = ldsT;
@@ -388,6 +412,8 @@ mpq_status fp8_quant_block_128x128(mpq_handle h, const void *w, int64_t rows, in
         return MPQ_OK;
     if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
         return MPQ_ERR_SHAPE;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     mpq::QuantArgs a{};
     a.rows = rows; a.cols = cols;
     a.q = q; a.ldq = ldq; a.s = s; a.lds = lds;
@@ -445,6 +471,8 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
         return MPQ_ERR_SHAPE;
     if (M == 0)
         return MPQ_OK;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     CUtensorMap tmA, tmB;
     if ((st = encode_operand(&tmA, A, M, K, lda, 128)) != MPQ_OK)
         return st;
@@ -473,6 +501,15 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
         sk = h->sk_mode == 2 || 10 * (waves * units - tiles) > waves * units;
     }
     if (sk) {
+        // The flags hold the epoch of the launch that last wrote them; a waiter accepts a
+        // flag >= its own epoch.  Before the counter would overflow, the flags are cleared
+        // (in stream order, ahead of the launch) and the count restarts.
+        if (h->sk_epoch == INT32_MAX) {
+            if (cudaMemsetAsync(h->d_sk_flags, 0, static_cast<size_t>(h->num_sms) * 8 * sizeof(int),
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                return MPQ_ERR_CUDA;
+            h->sk_epoch = 0;
+        }
         a.sk_part = h->d_sk_part;
         a.sk_flags = h->d_sk_flags;
         a.sk_epoch = ++h->sk_epoch;
@@ -489,6 +526,8 @@ static mpq_status launch_fused_grouped(mpq_handle h, void *workspace, int64_t G,
                                        const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb, void *C,
                                        int64_t ldc, int out_dtype, uint32_t flags, void *stream)
 {
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     uint8_t *xq = static_cast<uint8_t *>(workspace);
     float *sx = reinterpret_cast<float *>(xq + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
     int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
@@ -620,6 +659,8 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
         return MPQ_ERR_ALIGN;
     if (M_total == 0)
         return MPQ_OK;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     // Row tiles by default: on single-SM tiles they stream the weights at the HBM rate even
     // for a few tokens per expert; weight tiles only on request.
     const bool weight_tiles = (flags & MPQ_GROUPED_WEIGHT_TILES) != 0;
@@ -658,6 +699,8 @@ mpq_status mpq_selftest_wait_timeout(mpq_handle h, uint64_t timeout_ns, void *st
 {
     if (h == nullptr)
         return MPQ_ERR_NULL;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
     return from_cuda(mpq::launch_wait_selftest(h->d_status, timeout_ns == 0 ? 1000000ull : timeout_ns,
                                                static_cast<cudaStream_t>(stream)));
 }

@@ -474,14 +474,9 @@ cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const 
     void (*kern)(CUtensorMap, CUtensorMap, GemmArgs, FuseArgs) =
         ki == 0 ? decode_kernel<false, false> : ki == 1 ? decode_kernel<true, false>
                 : ki == 2 ? decode_kernel<false, true> : decode_kernel<true, true>;
-    static bool configured[4] = {false, false, false, false};
-    if (!configured[ki]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kDSmem));
-        if (e != cudaSuccess)
-            return e;
-        configured[ki] = true;
-    }
+    static std::atomic<uint64_t> configured[4];   // per variant: devices already set up
+    if (cudaError_t e = ensure_max_dyn_smem(kern, kDSmem, configured[ki]); e != cudaSuccess)
+        return e;
     const FuseArgs none{};
     if (fuse == nullptr) {
         kern<<<grid, kDThreads, kDSmem, st>>>(tmX, tmW, a, none);

@@ -686,14 +686,9 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
 {
     auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE, SK>;
     const size_t smem = smem_bytes<PAIR>(GR);
-    static bool configured = false;  // one attribute call per instantiation and process
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};   // per instantiation: devices already set up
+    if (cudaError_t e = ensure_max_dyn_smem(kern, smem, configured); e != cudaSuccess)
+        return e;
     if (!PAIR && !FUSE) {
         kern<<<grid, kThreads, smem, st>>>(tmA, tmB, tmC, a, f);
         return cudaGetLastError();

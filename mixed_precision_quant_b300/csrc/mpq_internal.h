@@ -1,6 +1,7 @@
 // mpq_internal.h -- launchers shared between the C-ABI layer and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -123,5 +124,24 @@ cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const 
                           const FuseArgs *fuse, int num_sms, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);
+
+// Dynamic shared memory above 48 KB is enabled per kernel and per device (the attribute
+// belongs to the kernel's module in that device's context).  `done` caches, one bit per
+// device (devices 0..63; others set the attribute on every call), that it has been set.
+template <class Kern>
+cudaError_t ensure_max_dyn_smem(Kern kern, size_t smem, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess && bit != 0)
+        done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 } // namespace mpq

@@ -42,7 +42,21 @@ def test_version_and_status_strings(lib):
     assert b"sm_103a" in lib.mpq_version()
     lib.mpq_status_string.restype = ctypes.c_char_p
     assert lib.mpq_status_string(6) == b"device-side wait timed out"
+    assert lib.mpq_status_string(8) == b"the current device is not the handle's device"
     assert lib.mpq_status_string(99) == b"unknown status"
+
+
+def test_every_status_code_has_a_string_in_the_library_and_the_binding(lib):
+    # the codes of the header's mpq_status enum, each with its own text on both sides
+    src = open(os.path.join(ROOT, "include", "mpq.h")).read()
+    codes = [int(v) for v in re.findall(r"MPQ_(?:OK|ERR_[A-Z]+)\s*=\s*(\d+)", src)]
+    assert codes == list(range(len(codes)))
+    lib.mpq_status_string.restype = ctypes.c_char_p
+    texts = [lib.mpq_status_string(c) for c in codes]
+    assert b"unknown status" not in texts and len(set(texts)) == len(texts)
+    binding = open(os.path.join(ROOT, "mixed_precision_quant_b300", "__init__.py")).read()
+    table = re.search(r"_STATUS = \{(.*?)\}", binding, flags=re.S).group(1)
+    assert sorted(int(k) for k in re.findall(r"(\d+):", table)) == codes
 
 
 def test_null_handle_rejected_before_any_cuda_call(lib):
