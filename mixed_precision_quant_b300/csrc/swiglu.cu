@@ -14,7 +14,8 @@
 // rounding; every step uses an explicitly rounded intrinsic, so no contraction changes it.
 //
 // Design: memory-bound (4 bytes read, ~1 byte written per output value).  A grid-stride
-// loop over (row, 128-column group) items; four consecutive lanes share a group, each
+// loop over (row, 128-column group) items, on one wave of resident blocks; four
+// consecutive lanes share a group, each
 // holding four 16-byte chunks of the gate and the matching four of the up half (coalesced
 // 64-byte pieces per load instruction), the group's max-abs combined by two shuffles (eight
 // or sixteen lanes per group were slower: the per-group scale work is repeated per lane).
@@ -164,13 +165,28 @@ cudaError_t launch_swiglu_quant(const SwigluArgs &a, bool pow2, int num_sms, cud
     const int64_t ngroups = a.rows * (a.width / 128);
     if (ngroups == 0)
         return cudaSuccess;
+    // One wave: as many blocks as the SMs hold at once.  Every block runs the same number of
+    // grid-stride iterations, so blocks beyond the resident ones would form a second, partial
+    // wave that leaves SMs idle at the end.
+    void (*kern)(const SwigluArgs) = pow2 ? swiglu_quant_kernel<true> : swiglu_quant_kernel<false>;
+    static std::atomic<int> resident[2][64];   // blocks per SM, per variant and device (0: unknown)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = dev >= 0 && dev < 64 ? resident[pow2][dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSwThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        per_sm = per_sm > 0 ? per_sm : 1;
+        if (dev >= 0 && dev < 64)
+            resident[pow2][dev].store(per_sm, std::memory_order_relaxed);
+    }
     const int64_t want = (ngroups * kSwLpg + kSwThreads - 1) / kSwThreads;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    if (pow2)
-        swiglu_quant_kernel<true><<<grid, kSwThreads, 0, st>>>(a);
-    else
-        swiglu_quant_kernel<false><<<grid, kSwThreads, 0, st>>>(a);
+    kern<<<grid, kSwThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
