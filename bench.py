@@ -47,6 +47,9 @@ FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 FP8_PER_BF16 = 2.0             # nominal dense ratio fp8 : bf16 (4.5 : 2.25 PFLOP/s)
 M_DENSE, K_DENSE, N_DENSE = 4096, 7168, 18432
+# the workload both arms report (the reference arm times a bounded sample of it per step)
+WORKLOAD_DENSE = ("dense Fprop step: 1x128 quant A[4096,7168] + 128x128 quant W[18432,7168] "
+                  "+ block-scaled FP8 GEMM 4096x18432x7168, BF16 out")
 
 
 def load_peaks():
@@ -332,8 +335,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32 accumulate, bf16 out",
         "data": "synthetic (seeded; shapes of the pages' model)",
-        "config": {"workload": "dense Fprop step: 1x128 quant A[4096,7168] + 128x128 quant W[18432,7168] "
-                               "+ block-scaled FP8 GEMM 4096x18432x7168, BF16 out",
+        "config": {"workload": WORKLOAD_DENSE,
                    "M": M, "N": N, "K": K, "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": 3 * args.steps,
@@ -602,8 +604,8 @@ def run_reference(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp64 oracle on fp8 e4m3 codes", "data": "synthetic",
-        "config": {"workload": "dense Fprop step (bounded sample): 1x128 quant A + 128x128 quant W + GEMM, "
-                               "M=4096 N=18432 K=7168", "M": M_DENSE, "N": N_DENSE, "K": K_DENSE},
+        "config": {"workload": WORKLOAD_DENSE, "M": M_DENSE, "N": N_DENSE, "K": K_DENSE,
+                   "parallelism": "replicas x1"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
