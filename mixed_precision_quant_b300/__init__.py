@@ -259,7 +259,8 @@ def _ensure_workspace(device: torch.device, nbytes: int):
     with _hlock:
         buf = _workspaces.get(idx)
         if buf is None or buf.numel() < nbytes:
-            torch.cuda.current_stream(device).synchronize()   # no call in flight still uses the old one
+            # no call in flight, on any stream of the device, still uses the old buffer
+            torch.cuda.synchronize(device)
             buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
             _workspaces[idx] = buf
             _check("mpq_set_workspace", _lib.mpq_set_workspace(h, _ptr(buf), buf.numel()))
