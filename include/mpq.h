@@ -298,9 +298,10 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  * handle's workspace (mpq_set_workspace, mpq_grouped_fused_workspace_bytes), then runs
  * the row-tile GEMM (single-SM tiles) on those codes -- or the weight-tile GEMM with
  * MPQ_GROUPED_WEIGHT_TILES; the output equals fp8_quant_tile_1x128 followed by this call
- * on the same tiling, bit for bit.
- * of its CTAs (one per SM) must be resident at once, so it fails with MPQ_ERR_CUDA when
- * the cooperative launch is refused (e.g. other work occupies SMs).
+ * on the same tiling, bit for bit.  The fused launch is cooperative: its GEMM phase waits
+ * for the quantization phase of every CTA, so all of its CTAs (one per SM) must be
+ * resident at once, and the call fails with MPQ_ERR_CUDA when the cooperative launch is
+ * refused (e.g. other work occupies SMs).
  * Returns MPQ_ERR_WORKSPACE without a workspace of sufficient size.
  * Requirements: 1 <= G <= 1024; N % 128 == 0; K % 128 == 0; alignment as for
  * fp8_gemm_blockscaled.

@@ -217,6 +217,7 @@ def fp8_quant_block_128x128(w: torch.Tensor, *, pow2: bool = False, transposed: 
 
 def _out(M, N, out_dtype, C, dev):
     if C is not None:
+        _check_output(C, out_dtype, M, N, dev)
         return C
     dt = torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16
     return torch.empty((M, N), dtype=dt, device=dev)
@@ -279,6 +280,7 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
     flags = {"auto": 0, "rows": GROUPED_ROW_TILES, "weights": GROUPED_WEIGHT_TILES}.get(tiles)
     if flags is None:
         raise ValueError("tiles: expected 'auto', 'rows' or 'weights'")
+    _check_expert_args(offsets, B, sB)
     if fuse_quant:
         # A is BF16 [M, K], quantized 1x128 inside the launch (pow2: power-of-2 scales)
         _cuda2d(A, torch.bfloat16, "A")
@@ -289,12 +291,6 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
         if pow2:
             raise ValueError("pow2 applies to fuse_quant=True only")
         _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
-    if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.dim() == 1 and offsets.is_contiguous()):
-        raise TypeError("offsets: expected a contiguous 1-D int64 CUDA tensor")
-    if not (B.is_cuda and B.dtype == torch.uint8 and B.dim() == 3 and B.is_contiguous()):
-        raise TypeError("B: expected a contiguous [G, N, K] uint8 CUDA tensor")
-    if not (sB.is_cuda and sB.dtype == torch.float32 and sB.dim() == 3 and sB.is_contiguous()):
-        raise TypeError("sB: expected a contiguous [G, N/128, K/128] float32 CUDA tensor")
     G, N, K = B.shape
     M = A.shape[0]
     if offsets.numel() != G + 1 or A.shape[1] != K:
@@ -311,26 +307,62 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
     return C
 
 
+def _check_expert_args(offsets: torch.Tensor, B: torch.Tensor, sB: torch.Tensor, device: bool = True):
+    """The expert ranges and weights of a grouped GEMM: dtype and layout, then (unless
+    ``device`` is False) the device, so that a wrong dtype is reported as such wherever the
+    tensor lives."""
+    if offsets.dtype != torch.int64 or offsets.dim() != 1 or not offsets.is_contiguous():
+        raise TypeError(f"offsets: expected a contiguous 1-D int64 tensor, got {offsets.dtype} {tuple(offsets.shape)}")
+    if B.dtype != torch.uint8 or B.dim() != 3 or not B.is_contiguous():
+        raise TypeError("B: expected a contiguous [G, N, K] uint8 tensor")
+    if sB.dtype != torch.float32 or sB.dim() != 3 or not sB.is_contiguous():
+        raise TypeError("sB: expected a contiguous [G, N/128, K/128] float32 tensor")
+    if not device:
+        return
+    if not (offsets.is_cuda and B.is_cuda and sB.is_cuda):
+        raise TypeError("offsets, B and sB must be CUDA tensors")
+    if not (offsets.device == B.device == sB.device):
+        raise ValueError("offsets, B and sB must be on one device")
+
+
+def _check_output(C: torch.Tensor, out_dtype: int, M: int, N: int, device: torch.device):
+    """A caller-given output: the dtype the kernel writes (float32 for OUT_FP32, bfloat16
+    for OUT_BF16), [M, N] with unit column stride, on the inputs' device."""
+    want = {OUT_FP32: torch.float32, OUT_BF16: torch.bfloat16}.get(out_dtype)
+    if want is None:
+        raise ValueError(f"out_dtype: expected OUT_BF16 or OUT_FP32, got {out_dtype}")
+    if C.dtype != want:
+        raise TypeError(f"C: out_dtype asks for {want}, got {C.dtype}")
+    if C.dim() != 2 or tuple(C.shape) != (M, N):
+        raise ValueError(f"C: expected shape {(M, N)}, got {tuple(C.shape)}")
+    if not C.is_cuda or C.device != device:
+        raise TypeError(f"C: expected a CUDA tensor on {device}, got {C.device}")
+
+
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def fp8_grouped_gemm_fused_quant_noalloc(offsets: torch.Tensor, X: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
                                          C: torch.Tensor, *, out_dtype: int = OUT_BF16, pow2: bool = False,
                                          stream=None):
-    """Fused 1x128 quantization + grouped weight-tile GEMM that allocates nothing: the
+    """Fused 1x128 quantization + row-tile grouped GEMM that allocates nothing: the
     quantized activations stay in the library's fixed scratch area (NOALLOC_SCRATCH_BYTES),
-    so the output ``C`` must be given.  For callers that must not allocate device memory
-    while they run.  Calls that overlap in time (other streams or threads) race on the one
-    scratch area; the first call per device should come before any stream capture."""
-    _cuda2d(X, torch.bfloat16, "X")
-    if not (B.is_cuda and B.dtype == torch.uint8 and B.dim() == 3 and B.is_contiguous()):
-        raise TypeError("B: expected a contiguous [G, N, K] uint8 CUDA tensor")
-    if not (sB.is_cuda and sB.dtype == torch.float32 and sB.dim() == 3 and sB.is_contiguous()):
-        raise TypeError("sB: expected a contiguous [G, N/128, K/128] float32 CUDA tensor")
+    so the output ``C`` must be given (float32 for OUT_FP32, bfloat16 for OUT_BF16).  For
+    callers that must not allocate device memory while they run.  Calls that overlap in
+    time (other streams or threads) race on the one scratch area; the first call per device
+    should come before any stream capture."""
+    _check_expert_args(offsets, B, sB, device=False)
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError(f"X: expected a 2-D bfloat16 tensor, got {X.dtype} {tuple(X.shape)}")
     G, N, K = B.shape
     M = X.shape[0]
-    if offsets.numel() != G + 1 or X.shape[1] != K or tuple(C.shape) != (M, N):
-        raise ValueError("shape mismatch between offsets, X, B and C")
+    if offsets.numel() != G + 1 or X.shape[1] != K:
+        raise ValueError("shape mismatch between offsets, X and B")
+    _check_output(C, out_dtype, M, N, B.device)
+    _check_expert_args(offsets, B, sB)
+    _cuda2d(X, torch.bfloat16, "X")
+    if X.device != B.device:
+        raise ValueError("X must be on the device of B")
     dev = X.device
     with torch.cuda.device(dev):   # the handle's device is current for the call
         st = _lib.fp8_grouped_gemm_fused_quant_noalloc(_handle(dev), G, _ptr(offsets), M, N, K, _ptr(X), _ld(X), _ptr(B),

@@ -277,33 +277,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// 2-D tiled load multicast to every CTA of `mask` in the cluster: the tile lands at the
-// same shared offset `dst` in each of them and completes `bytes` on the mbarrier at the
-// same offset `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar, int32_t x,
-                                               int32_t y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when every tcgen05
-// operation issued so far by this thread completes.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
-// ---------------------------------------------------------------- TMA stores
-
-// 2-D tiled store of a shared-memory box to global memory (clipped at the tensor bounds),
-// tracked by the executing thread's bulk async-group.
 // ---------------------------------------------------------------- CTA pairs (2-SM MMA)
 //
 // With cta_group::2 the even CTA of a cluster pair issues MMAs that read A and B from both
@@ -360,6 +333,10 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// ---------------------------------------------------------------- TMA stores
+
+// 2-D tiled store of a shared-memory box to global memory (clipped at the tensor bounds),
+// tracked by the executing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x, int32_t y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -99,9 +99,11 @@ struct FuseArgs {
 // Block-scaled FP8 GEMM on tcgen05: C[M,N] = sum over 128-wide K slices of
 // (A_slice B_slice^T) * sA * sB, promoted into FP32 after every slice.
 // tmA covers A [rows, K] E4M3, tmB covers B [rows, K] E4M3 (both K-major, 128B swizzle).
-// `pair`: 2-CTA clusters sharing B through multicast; each CTA then loads B in boxes of
+// `pair`: 2-CTA clusters computing 256 x 256 tiles with 2-SM MMAs (cta_group::2); each CTA
+// loads its own 128 rows of A and half of the tile's B rows, in boxes of
 // gemm_b_box_rows(true) = 128 rows, else 256.
-// tmC: output view [rows, N] (BF16 or FP32) with box 64 bytes x 32 rows, 64-byte swizzle.
+// tmC: output view [rows, N] (BF16 or FP32), boxes of 32 rows x 128 bytes with 128-byte
+// swizzle in pair mode, 32 rows x 64 bytes with 64-byte swizzle single-SM.
 // fuse != null: grouped GEMM with fused 1x128 activation quantization (single-SM tiles,
 // weight block scales): tmA must cover fuse->xq, a.sA / a.ldsa must be fuse->sx / M.
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
@@ -109,21 +111,21 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
                         const FuseArgs *fuse = nullptr);
 int gemm_b_box_rows(bool pair);
 
-// Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
 // Grouped GEMM for few tokens per expert (weights as the MMA's M operand, tokens as N):
 // tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
 // weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
 // the grouped launch_gemm (sB block scales [G][N/128][ldsb]); C is written directly.
-// Size of the fixed scratch area of fp8_grouped_gemm_fused_quant_noalloc (MPQ_NOALLOC_SCRATCH_BYTES),
-// and its device address on the current device (looked up on first use, then cached).
-constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
-cudaError_t noalloc_scratch(void **ptr);
-
 int decode_x_box_rows();
 cudaError_t launch_decode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &a, bool out_fp32,
                           const FuseArgs *fuse, int num_sms, cudaStream_t st);
 
+// Self-test of the bounded wait: one CTA waits on a barrier nobody arrives on.
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st);
+
+// Size of the fixed scratch area of fp8_grouped_gemm_fused_quant_noalloc (MPQ_NOALLOC_SCRATCH_BYTES),
+// and its device address on the current device (looked up on first use, then cached).
+constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
+cudaError_t noalloc_scratch(void **ptr);
 
 // Dynamic shared memory above 48 KB is enabled per kernel and per device (the attribute
 // belongs to the kernel's module in that device's context).  `done` caches, one bit per

@@ -44,17 +44,21 @@ def test_noalloc_matches_fused_entry_point(mpq, counts, lead, trail, N, K, pow2)
     M = x_cpu.shape[0]
     offs = torch.from_numpy(off.astype(np.int64)).cuda()
     x, qbd, sbd = x_cpu.cuda(), torch.from_numpy(qb).cuda(), torch.from_numpy(sb).cuda()
-    ref_gpu = torch.full((M, N), -5.0, dtype=torch.float32, device="cuda")
-    mpq.fp8_grouped_gemm_blockscaled(offs, x, None, qbd, sbd, out_dtype=mpq.OUT_FP32, C=ref_gpu, fuse_quant=True,
+    # the entry point with a workspace (same launch, same tiling): the results must agree
+    # bit for bit, as the header promises
+    fused = torch.full((M, N), -5.0, dtype=torch.float32, device="cuda")
+    mpq.fp8_grouped_gemm_blockscaled(offs, x, None, qbd, sbd, out_dtype=mpq.OUT_FP32, C=fused, fuse_quant=True,
                                      pow2=pow2)
-    ref = ref_gpu.cpu().numpy().astype(np.float64)
-    _, absref = oracle.grouped_gemm_ref(off, *oracle.quant_tile_1x128(bf16_bits(x_cpu), pow2=pow2), qb, sb)
+    # the oracle: 1x128 quantization of the BF16 rows, then the FP64 grouped GEMM
+    ref, absref = oracle.grouped_gemm_ref(off, *oracle.quant_tile_1x128(bf16_bits(x_cpu), pow2=pow2), qb, sb)
     rows = np.zeros(M, bool)
     rows[int(off[0]):int(off[-1])] = True
+    assert_gemm_close(fused.cpu().numpy()[rows], ref[rows], absref[rows], "fused entry point")
     for call in range(2):   # two calls in a row reuse the same scratch area
         C = torch.full((M, N), -5.0, dtype=torch.float32, device="cuda")
         mpq.fp8_grouped_gemm_fused_quant_noalloc(offs, x, qbd, sbd, C, out_dtype=mpq.OUT_FP32, pow2=pow2)
         torch.cuda.synchronize()
+        assert torch.equal(C, fused), f"no-alloc call {call} differs from the fused entry point"
         got = C.cpu().numpy().astype(np.float64)
         assert_gemm_close(got[rows], ref[rows], absref[rows], f"no-alloc call {call}")
         assert np.all(got[~rows] == -5.0), "rows outside every expert were written"
