@@ -11,9 +11,9 @@ arrays.  Every function cites, in the C source, the passage of the source pages
 it follows.  Pins that tie it to something other than itself are in
 ``tests/test_oracle_pins.py``.
 
-Parity status: every function here is pinned (see the tests); the error-versus-K
-study (``gemm_bf16_fp64``) is a report against unquantized inputs and is not a
-parity gate.
+Parity status: every function here is pinned (see the tests).  The error-versus-K
+study of the benchmark is a report against the unquantized inputs, computed there,
+and is not a parity gate.
 """
 from __future__ import annotations
 
@@ -81,8 +81,6 @@ def _load():
         lib.mpqo_gemm_ref_at.argtypes = [ctypes.c_int, I, P, I, P, I, P, I, P, I, P, P, I, P, P]
         lib.mpqo_grouped_gemm_ref.restype = None
         lib.mpqo_grouped_gemm_ref.argtypes = [I, P, I, I, P, I, P, I, P, I, P, I, P, P, I]
-        lib.mpqo_gemm_bf16_fp64.restype = None
-        lib.mpqo_gemm_bf16_fp64.argtypes = [I, I, I, P, I, P, I, P, I]
         _lib = lib
         return lib
 
@@ -261,13 +259,3 @@ def grouped_gemm_ref(offsets, qa, sa, qb, sb):
     _load().mpqo_grouped_gemm_ref(G, _ptr(off), N, K, _ptr(qa), K, _ptr(sa), sa.shape[1],
                                   _ptr(qb), K, _ptr(sb), sb.shape[2], _ptr(ref), _ptr(absref), N)
     return ref, absref
-
-
-def gemm_bf16_fp64(x_bf16_bits: np.ndarray, w_bf16_bits: np.ndarray) -> np.ndarray:
-    """Unquantized reference sum_k x[m,k] w[n,k] in FP64 (error-versus-K report)."""
-    x = _c(x_bf16_bits, np.uint16); w = _c(w_bf16_bits, np.uint16)
-    M, K = x.shape
-    N = w.shape[0]
-    ref = np.empty((M, N), np.float64)
-    _load().mpqo_gemm_bf16_fp64(M, N, K, _ptr(x), K, _ptr(w), K, _ptr(ref), N)
-    return ref

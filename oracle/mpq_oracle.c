@@ -419,16 +419,3 @@ void mpqo_grouped_gemm_ref(int64_t G, const int64_t *off, int64_t N, int64_t K,
                       ref + m0 * ldr, absref + m0 * ldr, ldr);
     }
 }
-
-/* Unquantized FP64 reference on BF16 inputs: sum_k x[m,k] w[n,k]. */
-void mpqo_gemm_bf16_fp64(int64_t M, int64_t N, int64_t K, const uint16_t *X, int64_t ldx,
-                         const uint16_t *W, int64_t ldw, double *ref, int64_t ldr)
-{
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t n = 0; n < N; ++n) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < K; ++k)
-                acc += (double)bf16_to_float(X[m * ldx + k]) * (double)bf16_to_float(W[n * ldw + k]);
-            ref[m * ldr + n] = acc;
-        }
-}

@@ -452,6 +452,48 @@ def test_requant_zero_and_signed_zero_groups():
 
 
 
+def _read_requant_golden():
+    """tests/golden/requant_128x1_worked.txt: a hand-worked tile whose binary32 rounding of
+    dec(q) * s decides one code (column 0) and one scale (column 1)."""
+    q = np.zeros((128, 128), np.uint8)
+    s = np.ones((1, 128), np.float32)
+    expect = {}
+    with open(os.path.join(GOLDEN, "requant_128x1_worked.txt")) as f:
+        for line in f:
+            tok = line.split("#", 1)[0].split()
+            if not tok:
+                continue
+            if tok[0] == "scale_in":
+                s[0, int(tok[1])] = np.array([int(tok[2], 16)], np.uint32).view(np.float32)[0]
+            elif tok[0] == "code_in":
+                q[int(tok[1]), int(tok[2])] = int(tok[3], 16)
+            elif tok[0] == "expect":
+                rule = expect.setdefault(tok[1], {"scale": {}, "code": {}})
+                if tok[2] == "scale":
+                    rule["scale"][int(tok[3])] = int(tok[4], 16)
+                else:
+                    rule["code"][(int(tok[3]), int(tok[4]))] = int(tok[5], 16)
+    return q, s, expect
+
+
+@pytest.mark.parametrize("rule", ["amax", "pow2"])
+def test_golden_requant_binary32_dequantization(rule):
+    """The dequantized value is one binary32 product: with exact (or FP64) products the
+    code of column 0, row 1 would be 0x39 and the amax-rule scale of column 1 would be
+    0x3F92492C."""
+    q, s, expect = _read_requant_golden()
+    qT, sT = oracle.requant_tile_128x1(q, s, pow2=(rule == "pow2"))
+    want_s = np.ones(128, np.float32).view(np.uint32)
+    for c, bits in expect[rule]["scale"].items():
+        want_s[c] = bits
+    assert np.array_equal(sT[0].view(np.uint32), want_s)
+    want_q = np.zeros((128, 128), np.uint8)
+    for (c, t), code in expect[rule]["code"].items():
+        want_q[c, t] = code
+    assert np.array_equal(qT, want_q)
+
+
+
 # ------------------------------------------------------ SwiGLU + quantization
 
 def _ulp32(v):
@@ -544,3 +586,37 @@ def test_swiglu_quant_error_bound(pow2):
     slack = 1 + 2.0 ** -18
     assert np.all(err[normal] <= 2.0 ** -4 * np.abs(x[normal]) * slack + 8 * _ulp32(x[normal]))
     assert np.all(err[~normal] <= 2.0 ** -10 * srow[~normal] * slack + 8 * _ulp32(x[~normal]))
+
+
+def _read_swiglu_golden():
+    groups = {}
+    cur = None
+    with open(os.path.join(GOLDEN, "swiglu_1x128_worked.txt")) as f:
+        for line in f:
+            tok = line.split("#", 1)[0].split()
+            if not tok:
+                continue
+            if tok[0] == "group":
+                cur = tok[1]
+                groups[cur] = {"scale": int(tok[2], 16), "elems": []}
+            else:
+                groups[cur]["elems"].append(tuple(int(t, 0) for t in tok))
+    return groups
+
+
+def test_golden_swiglu_binary32_sequence():
+    """silu(g) * u is a sequence of binary32 operations, each rounded once: computing it in
+    FP64 and rounding once would give the scales 0x3D65B6DA and 0x3B80D919 instead."""
+    groups = _read_swiglu_golden()
+    assert set(groups) == {"P", "Q"}
+    names = sorted(groups)
+    h = np.zeros((len(names), 256), np.uint16)
+    want_q = np.zeros((len(names), 128), np.uint8)
+    for r, name in enumerate(names):
+        for i, gate, up, code in groups[name]["elems"]:
+            h[r, i], h[r, 128 + i] = gate, up
+            want_q[r, i] = code
+    q, sc = oracle.swiglu_quant_1x128(h, pow2=False)
+    assert np.array_equal(q, want_q)
+    for r, name in enumerate(names):
+        assert sc[0, r].view(np.uint32) == groups[name]["scale"], name
