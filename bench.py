@@ -367,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     fp8_cublas = measure_fp8_cublas(dev)
     cub = fp8_cublas.get("8192x8192x8192")
-    groups = set(args.rows.split(",")) if args.rows else {"backward", "moe", "accuracy"}
+    groups = set(args.rows.split(",")) if args.rows else {"backward", "moe", "mx", "accuracy"}
     rows = {} if args.no_rows else measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups)
 
     result = {
@@ -525,13 +525,18 @@ def accuracy_vs_k(mpq, workloads, dev, ks=(512, 1024, 2048, 4096, 8192, 16384), 
         scale = st_a.double() * st_w.double()
         tens = err((ta @ tw.T) * scale)
         tens14 = err(_acc_limited(ta, tw, bits) * scale)
+        # power-of-2 scales on both operands, the microscaling GEMM (whole K in TMEM)
+        pqa, psa, _, _ = mpq.fp8_quant_tile_1x128(a, pow2=True)
+        pqw, _, psw = mpq.fp8_quant_block_128x128(w, pow2=True)
+        cmx = mpq.fp8_gemm_mx_pow2(mpq.FPROP, pqa, psa, pqw, psw, out_dtype=mpq.OUT_FP32)
         row["schemes"] = {"fine_grained_promoted": err(c), "fine_grained_14bit_slices": fine14,
-                          "tensorwise_fp32_acc": tens, "tensorwise_14bit_acc": tens14}
+                          "tensorwise_fp32_acc": tens, "tensorwise_14bit_acc": tens14,
+                          "fine_grained_pow2_mx": err(cmx)}
         out.append(row)
     return out
 
 
-def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe", "accuracy")):
+def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe", "mx", "accuracy")):
     """Time every other hot-path step on its configuration (CUDA events, L2 flushed).
     ``groups`` selects the backward-pair rows, the MoE rows and the accuracy report."""
     hbm = peaks["hbm_gbs"]
@@ -545,9 +550,53 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe"
         _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)
     if "moe" in groups:
         _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)
+    if "mx" in groups:
+        _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)
     if "accuracy" in groups:
         out["accuracy_vs_K"] = accuracy_vs_k(mpq, workloads, dev)
     return out
+
+
+def _mx_rows(mpq, workloads, dev, flush, fp8_peak, out):
+    """Power-of-2 scales on both operands: the microscaling GEMM (scales applied by the
+    tensor cores, the whole K accumulated in TMEM) against the software promotion path on
+    the same codes and scales, for the dense Fprop shape and the backward pair."""
+    import torch
+
+    def row(name, op, qa, sa, qb, sb, od, flops):
+        C = torch.empty((qa.shape[0], qb.shape[0]), dtype=torch.float32 if od == mpq.OUT_FP32 else torch.bfloat16,
+                        device=dev)
+        ms_mx = timed(lambda: mpq.fp8_gemm_mx_pow2(op, qa, sa, qb, sb, out_dtype=od, C=C), flush)
+        ms_sw = timed(lambda: mpq.fp8_gemm_blockscaled(op, qa, sa, qb, sb, out_dtype=od, C=C), flush)
+        st, where = mpq.mpq_check_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at {where:#x} in {name}")
+        tf_mx, tf_sw = flops / ms_mx / 1e9, flops / ms_sw / 1e9
+        out[name] = {"ms": round(ms_mx, 4), "TFLOPs": round(tf_mx, 1), "frac_fp8_peak": round(tf_mx / fp8_peak, 4),
+                     "software_promotion_ms": round(ms_sw, 4), "software_promotion_TFLOPs": round(tf_sw, 1),
+                     "bound": "tensor", "scales": "power of 2 on both operands"}
+
+    d = workloads.dense_fprop(device=dev)
+    qa, sa, _, _ = mpq.fp8_quant_tile_1x128(d["A"], pow2=True)
+    qb, _, sb = mpq.fp8_quant_block_128x128(d["W"], pow2=True)
+    M, K = qa.shape
+    N = qb.shape[0]
+    del d
+    row("mx_fprop_4096x18432x7168", mpq.FPROP, qa, sa, qb, sb, mpq.OUT_BF16, 2.0 * M * N * K)
+    del qa, sa, qb, sb
+    torch.cuda.empty_cache()
+    d = workloads.backward_pair(device=dev)
+    dY, X, Wl = d["dY"], d["X"], d["W"]
+    T, Nout = dY.shape
+    Kin = X.shape[1]
+    qdy, sdy, qdyT, sdyT = mpq.fp8_quant_tile_1x128(dY, pow2=True, transposed=True)
+    _, _, qxT, sxT = mpq.fp8_quant_tile_1x128(X, pow2=True, rows_out=False, transposed=True)
+    _, qwT, sw = mpq.fp8_quant_block_128x128(Wl, pow2=True, transposed=True)
+    fl = 2.0 * T * Kin * Nout
+    row("mx_dgrad_8192x7168x2048_fp32", mpq.DGRAD, qdy, sdy, qwT, sw, mpq.OUT_FP32, fl)
+    row("mx_wgrad_7168x2048x8192_fp32", mpq.WGRAD, qxT, sxT, qdyT, sdyT, mpq.OUT_FP32, fl)
+    del d, dY, X, Wl, qdy, sdy, qdyT, sdyT, qxT, sxT, qwT, sw
+    torch.cuda.empty_cache()
 
 
 def _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
@@ -821,7 +870,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--rows", default="", help="comma list of row groups to measure: backward, moe, accuracy "
+    ap.add_argument("--rows", default="", help="comma list of row groups to measure: backward, moe, mx, accuracy "
                     "(default: all)")
     ap.add_argument("--profile", choices=PROFILE_CASES, default=None,
                     help="launch one kernel on a small case for an ncu capture (no timing, no JSON line)")

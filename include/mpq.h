@@ -54,8 +54,11 @@ typedef enum mpq_status {
     MPQ_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed                       */
     MPQ_ERR_TIMEOUT = 6,     /* a device-side wait ran out (reported by the status word)  */
     MPQ_ERR_WORKSPACE = 7,   /* no workspace set on the handle, or it is too small        */
-    MPQ_ERR_DEVICE = 8       /* the current CUDA device is not the one the handle was
+    MPQ_ERR_DEVICE = 8,      /* the current CUDA device is not the one the handle was
                                 created on (nothing was launched)                         */
+    MPQ_ERR_SCALE = 9        /* a scale given to fp8_gemm_mx_pow2 is not a power of 2 in
+                                2^-127 .. 2^127 (found on the device, reported by the
+                                status word; that call's output is not valid)             */
 } mpq_status;
 
 typedef enum mpq_op {
@@ -263,6 +266,34 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
                                 const uint8_t *A, int64_t lda, const float *sA, int64_t ldsa,
                                 const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
                                 void *C, int64_t ldc, int out_dtype, void *stream);
+
+/*
+ * fp8_gemm_mx_pow2 -- the block-scaled FP8 GEMM of fp8_gemm_blockscaled for operands whose
+ * scales are all integral powers of 2 (page 4, second paragraph), with the scales applied
+ * by the tensor cores' microscaling MMA (page 3, first paragraph: the tensor cores of this
+ * GPU generation support microscaling formats with small quantization groups):
+ * tcgen05.mma kind::mxf8f6f4.block_scale with UE8M0 scale factors, one per 32-element K
+ * block (each 128-K slice's scale repeated over its four blocks).  The MMAs accumulate the
+ * scaled products of the whole K in FP32 in TMEM, so no slice is promoted by CUDA-core
+ * FMAs: with power-of-2 scales each scaled product is exact, and the per-slice promotion of
+ * the software path becomes part of the tensor cores' FP32 accumulation.
+ *
+ *   Same arguments, layouts, ops (MPQ_OP_FPROP / DGRAD / WGRAD), output types and
+ *   requirements as fp8_gemm_blockscaled, and the same sum.
+ *   Every scale read (sA for rows < M, sB for columns < N) must be a power of 2 between
+ *   2^-127 and 2^127 -- as the quantizers write with MPQ_POW2 for any group whose max-abs
+ *   value is at least 2^-119 (smaller nonzero groups get smaller scales).  The kernel checks
+ *   each scale; one that is not representable records MPQ_ERR_SCALE in the handle's status
+ *   word (mpq_check_device_status) and the output of that call is not valid.
+ * Tiling: 2-SM pair tiles of 256 x 256 (mpq_set_gemm_cta_pair does not apply), a
+ * data-parallel schedule (mpq_set_gemm_stream_k does not apply).  Results agree with
+ * fp8_gemm_blockscaled within the GEMM tolerance of the method, not bit for bit (the FP32
+ * sums are rounded in another order).  Asynchronous on `stream`; nothing is allocated.
+ */
+mpq_status fp8_gemm_mx_pow2(mpq_handle h, int op, int64_t M, int64_t N, int64_t K,
+                            const uint8_t *A, int64_t lda, const float *sA, int64_t ldsa,
+                            const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                            void *C, int64_t ldc, int out_dtype, void *stream);
 
 /*
  * fp8_grouped_gemm_blockscaled -- MoE expert GEMMs (page 2, first paragraph: large

@@ -29,7 +29,8 @@ FUSE_QUANT_A = 8
 _STATUS = {0: "ok", 1: "null pointer argument", 2: "invalid size or leading dimension",
            3: "misaligned pointer or stride", 4: "unsupported op, dtype or flags",
            5: "CUDA call failed", 6: "device-side wait timed out", 7: "no workspace set, or too small",
-           8: "the current device is not the handle's device"}
+           8: "the current device is not the handle's device",
+           9: "a scale is not a power of 2 in the UE8M0 range"}
 
 
 class MPQError(RuntimeError):
@@ -59,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "fp8_requant_tile_128x1": (INT, [P, P, I, I, I, P, I, P, I, P, I, U32, P]),
         "fp8_swiglu_quant_1x128": (INT, [P, P, I, I, I, P, I, P, I, U32, P]),
         "fp8_gemm_blockscaled": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
+        "fp8_gemm_mx_pow2": (INT, [P, INT, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, P]),
         "fp8_grouped_gemm_blockscaled": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, INT, U32, P]),
         "mpq_selftest_wait_timeout": (INT, [P, U64, P]),
         "mpq_set_workspace": (INT, [P, P, ctypes.c_size_t]),
@@ -242,6 +244,27 @@ def fp8_gemm_blockscaled(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Te
                                        _ld(B), _ptr(sB), _ld(sB), _ptr(C), _ld(C), int(out_dtype),
                                        _stream(dev, stream))
     _check("fp8_gemm_blockscaled", st)
+    return C
+
+
+def fp8_gemm_mx_pow2(op: int, A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor, *,
+                     out_dtype: int = OUT_BF16, C: Optional[torch.Tensor] = None, stream=None):
+    """The GEMM of :func:`fp8_gemm_blockscaled` for power-of-2 scales (2^-127 .. 2^127), with
+    the scales applied by the tensor cores' microscaling MMA and the whole K accumulated in
+    FP32 by the tensor cores.  Same arguments and layouts.  A scale outside that set is
+    reported by :func:`mpq_check_device_status` (status 9)."""
+    _cuda2d(A, torch.uint8, "A"); _cuda2d(B, torch.uint8, "B")
+    _cuda2d(sA, torch.float32, "sA"); _cuda2d(sB, torch.float32, "sB")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    dev = A.device
+    C = _out(M, N, out_dtype, C, dev)
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_gemm_mx_pow2(_handle(dev), int(op), M, N, K, _ptr(A), _ld(A), _ptr(sA), _ld(sA), _ptr(B),
+                                   _ld(B), _ptr(sB), _ld(sB), _ptr(C), _ld(C), int(out_dtype), _stream(dev, stream))
+    _check("fp8_gemm_mx_pow2", st)
     return C
 
 

@@ -150,6 +150,7 @@ const char *mpq_status_string(int s)
     case MPQ_ERR_TIMEOUT: return "device-side wait timed out";
     case MPQ_ERR_WORKSPACE: return "no workspace set, or too small";
     case MPQ_ERR_DEVICE: return "the current device is not the handle's device";
+    case MPQ_ERR_SCALE: return "a scale is not a power of 2 in the UE8M0 range";
     default: return "unknown status";
     }
 }
@@ -516,6 +517,45 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     }
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, pair, h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+mpq_status fp8_gemm_mx_pow2(mpq_handle h, int op, int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                            const float *sA, int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB,
+                            int64_t ldsb, void *C, int64_t ldc, int out_dtype, void *stream)
+{
+    if (h == nullptr)
+        return MPQ_ERR_NULL;
+    if (op != MPQ_OP_FPROP && op != MPQ_OP_DGRAD && op != MPQ_OP_WGRAD)
+        return MPQ_ERR_UNSUPPORTED;
+    mpq_status st = check_gemm_common(N, K, A, lda, sA, B, ldb, sB, C, ldc, out_dtype);
+    if (st != MPQ_OK)
+        return st;
+    if (M < 0 || M > (int64_t(1) << 31) || ldsa < M)
+        return MPQ_ERR_SHAPE;
+    if ((op == MPQ_OP_FPROP && ldsb < K / 128) || (op == MPQ_OP_DGRAD && ldsb < N / 128) ||
+        (op == MPQ_OP_WGRAD && ldsb < N))
+        return MPQ_ERR_SHAPE;
+    if (M == 0)
+        return MPQ_OK;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
+    CUtensorMap tmA, tmB, tmC;
+    if ((st = encode_operand(&tmA, A, M, K, lda, 128)) != MPQ_OK)
+        return st;
+    if ((st = encode_operand(&tmB, B, N, K, ldb, 128)) != MPQ_OK)
+        return st;
+    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32, true)) != MPQ_OK)
+        return st;
+    mpq::GemmArgs a{};
+    a.M = M; a.N = N; a.K = K;
+    a.sA = sA; a.ldsa = ldsa;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = 0;
+    a.C = C; a.ldc = ldc;
+    a.offsets = nullptr; a.G = 1;
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
+    return from_cuda(mpq::launch_gemm_mx(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, h->num_sms,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 // Fused grouped GEMM after validation: carve the workspace (codes [M, K], scales [K/128][M],

@@ -95,6 +95,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// The same bounded wait for a waiter with nothing else to do for a long time (e.g. an
+// epilogue warp during a tile's main loop): each try_wait asks the hardware to suspend the
+// thread until the phase completes or about 20 us pass, so the waiting warp takes no issue
+// slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, const WaitCtl &c, int tag)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_suspend(bar, parity)) {
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            if (c.status != nullptr && atomicCAS(c.status, 0, kStatusTimeout) == 0)
+                atomicExch(c.status + 1, tag);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- TMA / cp.async
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
@@ -331,6 +364,89 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster)
         : "memory");
+}
+
+// ---------------------------------------------------------------- microscaling MMA
+//
+// kind::mxf8f6f4 with block scaling: the tensor cores multiply each 32-element K block of
+// A row m by 2^(SFA(m) - 127) and of B column n by 2^(SFB(n) - 127) (UE8M0 scale factors,
+// read from TMEM) while accumulating in FP32.  Scale-factor layout in TMEM used here (one
+// 32-bit word per scale, its four bytes equal, so every K block of a 128-K slice takes the
+// same scale and the byte selectors of the instruction descriptor stay 0): the word of A
+// row m sits in column base + m/32 of lane m % 32, and the word of B column n in column
+// base + 4 + n/32 of lane n % 32, repeated in all four 32-lane quadrants of TMEM.
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: D = F32, A = B = E4M3 (K-major),
+// UE8M0 scale factors (bit 23), scale-factor byte selectors (bits 4-5 for B, 29-30 for A) 0.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n)
+{
+    return (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
+           | (1u << 23)                             // scale-factor type UE8M0
+           | (static_cast<uint32_t>(m >> 4) << 24); // M >> 4
+}
+
+// D[tmem] (+)= (A * 2^SFA) (B * 2^SFB)^T over both CTAs of the pair (one thread of the even CTA).
+__device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte matrix stored row after row (no swizzle:
+// 8-row core matrices of 128 bytes, 128 bytes apart), the source of tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(128 >> 4) << 16;             // leading byte offset (one 16-byte column)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;             // stride byte offset: 8 rows x 16 bytes
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
+    return d;                                               // swizzle mode 0: none
+}
+
+// Copy a 32-row x 16-byte shared-memory matrix into TMEM columns taddr .. taddr + 3, row r
+// into lane r of each of the four 32-lane quadrants (both CTAs of the pair, each from its own
+// shared memory).  Issued by one thread; ordered with that thread's MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Stores of registers into TMEM: 32 lanes (the warp's quadrant) x 4 or 8 consecutive columns.
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// Wait until this thread's TMEM stores have completed.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// UE8M0 code of a power-of-2 scale: the binary32 exponent field of a positive normal power
+// of 2 (2^-126 .. 2^127), or 0 for 2^-127; anything else is not representable and sets `bad`
+// (the code 127, scale 1, is returned in its place).
+__device__ __forceinline__ uint32_t ue8m0_of(float s, bool &bad)
+{
+    const uint32_t b = __float_as_uint(s);
+    const uint32_t e = (b >> 23) & 0xFFu;
+    if ((b & 0x807FFFFFu) == 0 && e >= 1 && e <= 254)
+        return e;
+    if (b == 0x00400000u)
+        return 0;
+    bad = true;
+    return 127;
 }
 
 // ---------------------------------------------------------------- TMA stores

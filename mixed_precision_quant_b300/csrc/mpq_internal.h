@@ -111,6 +111,11 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
                         const FuseArgs *fuse = nullptr);
 int gemm_b_box_rows(bool pair);
 
+// The same GEMM for power-of-2 scales on the microscaling MMA (kind::mxf8f6f4.block_scale):
+// 2-SM pair tiles of 256 x 256, tmA / tmB in boxes of 128 rows, tmC as in pair mode.
+cudaError_t launch_gemm_mx(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
+                           int scale_b, bool out_fp32, int num_sms, cudaStream_t st);
+
 // Grouped GEMM for few tokens per expert (weights as the MMA's M operand, tokens as N):
 // tmX covers the token codes [M, K] in boxes of decode_x_box_rows() rows, tmW the expert
 // weights [G*N, K] in boxes of 128 rows (both K-major, 128-byte swizzle).  Same GemmArgs as
