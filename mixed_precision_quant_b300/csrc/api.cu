@@ -491,6 +491,7 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     a.offsets = nullptr; a.G = 1;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
+    a.n_fastest = N < M ? 1 : 0;   // re-read the smaller operand (from L2)
     // Stream-K when the tiles fill more than one wave of CTAs (pairs) and, in the default
     // mode, the last wave would leave more than a tenth of the machine's time idle.
     const int64_t tile_m = pair ? 256 : 128;
@@ -554,6 +555,7 @@ mpq_status fp8_gemm_mx_pow2(mpq_handle h, int op, int64_t M, int64_t N, int64_t 
     a.offsets = nullptr; a.G = 1;
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
+    a.n_fastest = N < M ? 1 : 0;   // re-read the smaller operand (from L2)
     return from_cuda(mpq::launch_gemm_mx(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, h->num_sms,
                                          static_cast<cudaStream_t>(stream)));
 }

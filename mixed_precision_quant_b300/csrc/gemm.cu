@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Tile ti;
         int row0, rend;
         if (!GROUPED) {
-            const int mt = t % MT, nt = t / MT;
+            const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
             row0 = mt * C::TILE_M;
             rend = static_cast<int>(M);
             ti.g = 0;
@@ -323,8 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int g = lo;
             ti.g = g;
             const int local = t - gtile[g];
-            const int mtg = static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
-            const int nt = local / mtg, mt = local - nt * mtg;
+            const int rows_g = goff[g + 1] - goff[g];
+            const int mtg = (rows_g + C::TILE_M - 1) / C::TILE_M;
+            // an expert with more token rows than weight rows reads each row strip once and
+            // keeps its (smaller) weight in L2; otherwise each weight strip is read once
+            const bool nf = rows_g > N;
+            const int nt = nf ? local % NT : local / mtg, mt = nf ? local / NT : local - nt * mtg;
             row0 = goff[g] + mt * C::TILE_M;
             rend = goff[g + 1];
             ti.n0 = nt * BN;

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = unit, kb = warp;
             while (kb >= KB && t < T) { kb -= KB; t += nunits; }
             auto load = [&](int tt, int kk, float (&fa)[4], float (&fb)[8]) {
-                const int mt = tt % MT, nt = tt / MT;
+                const int mt = p.n_fastest ? tt / NT : tt % MT, nt = p.n_fastest ? tt % NT : tt / MT;
                 const int64_t row0 = static_cast<int64_t>(mt) * 256 + rank * 128;
                 const float *sa_row = p.sA + static_cast<int64_t>(kk) * p.ldsa;
 #pragma unroll
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------------------------------------------------- TMA producer
             uint32_t it = 0;
             for (int t = unit; t < T; t += nunits) {
-                const int mt = t % MT, nt = t / MT;
+                const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
                 const int row0 = mt * 256 + static_cast<int>(rank) * 128;
                 const int brow0 = nt * BN + static_cast<int>(rank) * 128;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
         uint32_t tc = 0;
         for (int t = unit; t < T; t += nunits, ++tc) {
-            const int mt = t % MT, nt = t / MT;
+            const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
             if (!mbar_wait_sleepy(bar(BAR_ACCFULL), tc & 1, ctl, 0x0900))
                 break;
             tc_fence_after();

@@ -81,6 +81,11 @@ struct GemmArgs {
     float4 *sk_part;            // [units][2][8 warps][32][32] float4
     int *sk_flags;              // [units][2][8 warps]
     int sk_epoch;
+    // Tile order: with n_fastest the output tiles of one row strip follow each other (each
+    // strip of A is read once while B stays in L2), else those of one column strip (each
+    // strip of B read once).  Dense GEMMs take the smaller operand as the one re-read;
+    // grouped GEMMs decide per expert (n-fastest when its rows outnumber its weight rows).
+    int n_fastest;
 };
 
 // Fused activation quantization: the token rows come as BF16 x [M, K] (ldx elements) and
