@@ -696,6 +696,19 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
                 res["swiglu_quant"] = {"ms": round(sms, 4), "GBps": round(gb(nbytes, sms), 1),
                                        "frac_hbm": round(gb(nbytes, sms) / hbm, 4), "bound": "hbm",
                                        "shape": [int(X.shape[0]), int(N)]}
+                # the same up projection with SwiGLU + pow2 quantization in the GEMM epilogue
+                # (one launch; the BF16 SwiGLU input is not written), against the two steps
+                # above (GEMM with BF16 output, then SwiGLU + quantization)
+                fused_args = (off, X, None, qw, sw) if name == "moe_decode" else (off, qx, sx, qw, sw)
+                efms = timed(lambda: mpq.fp8_grouped_gemm_swiglu_quant(*fused_args, pow2=True, q=sq, s=ss,
+                                                                       fuse_quant=name == "moe_decode"), flush)
+                two = (res[proj]["fused"]["ms"] if name == "moe_decode" else ms) + sms
+                res["up_swiglu_epilogue"] = {
+                    "ms": round(efms, 4), "two_step_ms": round(two, 4),
+                    "TFLOPs": round(fl / efms / 1e9, 1), "frac_fp8_peak": round(fl / efms / 1e9 / fp8_peak, 4),
+                    "path": ("one cooperative launch: 1x128 quantization of the BF16 rows + grouped GEMM + SwiGLU "
+                             "+ pow2 1x128 quantization" if name == "moe_decode" else
+                             "grouped GEMM with SwiGLU + pow2 1x128 quantization in the epilogue (codes + scales out)")}
                 del sq, ss
             total_ms += ms
             total_flops += fl
@@ -718,8 +731,8 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
 
 # ------------------------------------------------------------- profiling cases
 
-PROFILE_CASES = ("fprop", "dgrad", "wgrad", "grouped_up", "decode_fused", "decode_weights", "swiglu",
-                 "dual_x", "dual_dy", "block_t", "requant", "rows")
+PROFILE_CASES = ("fprop", "dgrad", "wgrad", "grouped_up", "grouped_up_swiglu", "decode_fused", "decode_fused_swiglu",
+                 "decode_weights", "swiglu", "dual_x", "dual_dy", "block_t", "requant", "rows", "mx_fprop")
 
 
 def run_profile(args):
@@ -739,11 +752,17 @@ def run_profile(args):
     u8, f32 = torch.uint8, torch.float32
     # every setup below avoids the profiled kernel, so that ncu's -s <warmup> skips exactly
     # the warm-up launches
-    if case in ("fprop", "rows"):
+    if case in ("fprop", "rows", "mx_fprop"):
         d = workloads.dense_fprop(device=dev)
         A = d["A"]
         M, K = A.shape
-        if case == "fprop":
+        if case == "mx_fprop":
+            qa, sa, _, _ = mpq.fp8_quant_tile_1x128(A, pow2=True)
+            qb, _, sb = mpq.fp8_quant_block_128x128(d["W"], pow2=True)
+            del d["W"]
+            C = torch.empty((M, qb.shape[0]), dtype=torch.bfloat16, device=dev)
+            launch = lambda: mpq.fp8_gemm_mx_pow2(mpq.FPROP, qa, sa, qb, sb, C=C)
+        elif case == "fprop":
             qa, sa, _, _ = mpq.fp8_quant_tile_1x128(A)
             qb, _, sb = mpq.fp8_quant_block_128x128(d["W"])
             del d["W"]
@@ -782,7 +801,7 @@ def run_profile(args):
             qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X)
             rqT, rsT = torch.empty((Kin, T), dtype=u8, device=dev), torch.empty((T // 128, Kin), dtype=f32, device=dev)
             launch = lambda: mpq.fp8_requant_tile_128x1(qx, sx, qT=rqT, sT=rsT)
-    elif case == "grouped_up":
+    elif case in ("grouped_up", "grouped_up_swiglu"):
         # the prefill routing restricted to every 8th expert (32 experts from the Zipf head to
         # the tail, 24611 rows, 769 on average: single-SM tiles as for the whole routing),
         # up projection 7168 -> 4096
@@ -798,8 +817,13 @@ def run_profile(args):
             mpq.fp8_quant_block_128x128(W[e], q=qw[e], s=sw[e])
         del W, X
         C = torch.empty((qx.shape[0], qw.shape[1]), dtype=torch.bfloat16, device=dev)
-        launch = lambda: mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qw, sw, C=C)
-    elif case in ("decode_fused", "decode_weights"):
+        if case == "grouped_up":
+            launch = lambda: mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qw, sw, C=C)
+        else:   # SwiGLU + pow2 quantization in the epilogue (codes and scales out)
+            sq_ = torch.empty((qx.shape[0], qw.shape[1] // 2), dtype=u8, device=dev)
+            ss_ = torch.empty((qw.shape[1] // 256, qx.shape[0]), dtype=f32, device=dev)
+            launch = lambda: mpq.fp8_grouped_gemm_swiglu_quant(off, qx, sx, qw, sw, q=sq_, s=ss_)
+    elif case in ("decode_fused", "decode_fused_swiglu", "decode_weights"):
         # the decode counts of the first 64 experts (1..256 tokens each), up projection
         counts = workloads.moe_decode_counts()[:64]
         off = workloads.offsets_from_counts(counts).to(dev)
@@ -814,6 +838,10 @@ def run_profile(args):
         C = torch.empty((X.shape[0], qw.shape[1]), dtype=torch.bfloat16, device=dev)
         if case == "decode_fused":
             launch = lambda: mpq.fp8_grouped_gemm_blockscaled(off, X, None, qw, sw, C=C, fuse_quant=True)
+        elif case == "decode_fused_swiglu":
+            sq_ = torch.empty((X.shape[0], qw.shape[1] // 2), dtype=u8, device=dev)
+            ss_ = torch.empty((qw.shape[1] // 256, X.shape[0]), dtype=f32, device=dev)
+            launch = lambda: mpq.fp8_grouped_gemm_swiglu_quant(off, X, None, qw, sw, q=sq_, s=ss_, fuse_quant=True)
         else:
             qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X)
             launch = lambda: mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qw, sw, C=C, tiles="weights")

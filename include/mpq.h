@@ -345,6 +345,48 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
                                         void *stream);
 
 /*
+ * fp8_grouped_gemm_swiglu_quant -- the MoE up projection with SwiGLU and the quantization of
+ * its result in the GEMM's epilogue: the FP8 input of the down projection leaves the GEMM
+ * directly, without the BF16 round trip through HBM (page 2, "9 Amazing Deepseek Hacks",
+ * the paragraphs on fusing the FP8 cast with the memory transfer: activations are read from
+ * HBM for quantization and written back only to be read again; page 1, first paragraph:
+ * the SwiGLU operator's inputs are cached and its output recomputed in the backward pass;
+ * page 4, second paragraph: this activation uses integral power-of-2 scales).
+ *
+ *   for expert g, rows m in [off[g], off[g+1]):
+ *     H[m, c]     = bf16( sum_kb (A_kb B_g[c]_kb^T) sA sB )        gate, c in [0, W)
+ *     H[m, W + c] = bf16( same with B_g[W + c] )                    up
+ *     x[m, c]     = silu(H[m, c]) * H[m, W + c]                     (as fp8_swiglu_quant_1x128)
+ *     q, s        = the 1x128 quantization of x (MPQ_POW2: power-of-2 scales)
+ *
+ *   d_offsets, G, M_total, K, A, lda, sA, ldsa, B, ldb, sB, ldsb as for
+ *              fp8_grouped_gemm_blockscaled with N = 2 W: B [G][2W][K] holds each expert's
+ *              gate weight rows [0, W) and up weight rows [W, 2W); sB [G][2W/128][ldsb].
+ *   H          BF16 [M_total, 2W], ldh >= 2W (device, written) or NULL: the SwiGLU input,
+ *              the values fp8_grouped_gemm_blockscaled would write with BF16 output (cached
+ *              for the backward pass's recomputation); not written when NULL.
+ *   q          [M_total, W] E4M3, ldq >= W (device, written);
+ *   s          [W/128][lds] float32, lds >= M_total (device, written).
+ *   flags      MPQ_POW2: power-of-2 scales for x (the pages' rule), else amax/448;
+ *              MPQ_FUSE_QUANT_A: A is BF16 [M_total, K] (lda in elements) quantized 1x128
+ *              with amax/448 scales inside the launch, as with fp8_grouped_gemm_blockscaled
+ *              (sA must be NULL; needs the handle's workspace; cooperative launch).
+ * Rows outside every expert are not written.  The codes, scales and H equal those of
+ * fp8_grouped_gemm_blockscaled (BF16 out, same tiling) followed by fp8_swiglu_quant_1x128,
+ * bit for bit.  Tiling as for fp8_grouped_gemm_blockscaled's row tiles (pair tiles when the
+ * experts average 2048 rows or more under the default mpq_set_gemm_cta_pair mode; single-SM
+ * tiles with MPQ_FUSE_QUANT_A).
+ * Requirements: 1 <= G <= 1024; W % 128 == 0; K % 128 == 0; A, B, q, H 16-byte aligned;
+ * lda, ldb, ldq % 16 == 0 (lda % 8 == 0 for BF16 A); ldh % 8 == 0; sA, sB, s 4-byte
+ * aligned.  Asynchronous on `stream`; nothing is allocated.
+ */
+mpq_status fp8_grouped_gemm_swiglu_quant(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
+                                         int64_t W, int64_t K, const void *A, int64_t lda, const float *sA,
+                                         int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                         void *H, int64_t ldh, uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                         uint32_t flags, void *stream);
+
+/*
  * fp8_grouped_gemm_fused_quant_noalloc -- fp8_grouped_gemm_blockscaled with
  * MPQ_FUSE_QUANT_A (fused 1x128 quantization of BF16 token rows, row-tile GEMM) that
  * allocates no memory and needs no workspace.  The source pages have no counterpart; it

@@ -66,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "mpq_set_workspace": (INT, [P, P, ctypes.c_size_t]),
         "mpq_grouped_fused_workspace_bytes": (INT, [I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
         "fp8_grouped_gemm_fused_quant_noalloc": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, INT, U32, P]),
+        "fp8_grouped_gemm_swiglu_quant": (INT, [P, I, P, I, I, I, P, I, P, I, P, I, P, I, P, I, P, I, P, I, U32, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -328,6 +329,49 @@ def fp8_grouped_gemm_blockscaled(offsets: torch.Tensor, A: torch.Tensor, sA: Opt
                                                int(out_dtype), flags, _stream(dev, stream))
     _check("fp8_grouped_gemm_blockscaled", st)
     return C
+
+
+def fp8_grouped_gemm_swiglu_quant(offsets: torch.Tensor, A: torch.Tensor, sA: Optional[torch.Tensor],
+                                  B: torch.Tensor, sB: torch.Tensor, *, pow2: bool = True, fuse_quant: bool = False,
+                                  H=False, q=None, s=None, stream=None):
+    """MoE up projection with SwiGLU and the 1x128 quantization of its result in the GEMM's
+    epilogue.  ``B [G, 2W, K]`` holds each expert's gate weight rows ``[0, W)`` and up weight
+    rows ``[W, 2W)``; ``A``/``sA`` as for :func:`fp8_grouped_gemm_blockscaled` (or BF16 ``A``
+    with ``fuse_quant=True``).  Returns ``(q [M, W] uint8, s [W/128, M] float32, H)`` where
+    ``H [M, 2W]`` BF16 is the SwiGLU input (gate | up), written when ``H`` is True (allocated)
+    or a tensor, else None.  ``pow2`` selects power-of-2 scales for the quantized result."""
+    _check_expert_args(offsets, B, sB)
+    G, N, K = B.shape
+    if N % 2:
+        raise ValueError("B: expected 2W rows per expert (gate then up)")
+    W = N // 2
+    if fuse_quant:
+        _cuda2d(A, torch.bfloat16, "A")
+        if sA is not None:
+            raise ValueError("sA must be None with fuse_quant=True")
+    else:
+        _cuda2d(A, torch.uint8, "A"); _cuda2d(sA, torch.float32, "sA")
+    M = A.shape[0]
+    if offsets.numel() != G + 1 or A.shape[1] != K:
+        raise ValueError("shape mismatch between offsets, A and B")
+    dev = A.device
+    q = q if q is not None else torch.empty((M, W), dtype=torch.uint8, device=dev)
+    s = s if s is not None else torch.empty((W // 128, M), dtype=torch.float32, device=dev)
+    if H is True:
+        H = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    elif H is False:
+        H = None
+    elif H is not None:
+        _check_output(H, OUT_BF16, M, N, dev)
+    flags = (POW2 if pow2 else 0) | (FUSE_QUANT_A if fuse_quant else 0)
+    if fuse_quant:
+        _ensure_workspace(dev, fused_workspace_bytes(M, K, G))
+    with torch.cuda.device(dev):   # the handle's device is current for the call
+        st = _lib.fp8_grouped_gemm_swiglu_quant(_handle(dev), G, _ptr(offsets), M, W, K, _ptr(A), _ld(A), _ptr(sA),
+                                                _ld(sA), _ptr(B), K, _ptr(sB), sB.shape[2], _ptr(H), _ld(H),
+                                                _ptr(q), _ld(q), _ptr(s), _ld(s), flags, _stream(dev, stream))
+    _check("fp8_grouped_gemm_swiglu_quant", st)
+    return q, s, H
 
 
 def _check_expert_args(offsets: torch.Tensor, B: torch.Tensor, sB: torch.Tensor, device: bool = True):

@@ -677,6 +677,75 @@ mpq_status fp8_grouped_gemm_fused_quant_noalloc(mpq_handle h, int64_t G, const i
                                 flags, stream);
 }
 
+mpq_status fp8_grouped_gemm_swiglu_quant(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
+                                         int64_t W, int64_t K, const void *A, int64_t lda, const float *sA,
+                                         int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB, int64_t ldsb,
+                                         void *H, int64_t ldh, uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                         uint32_t flags, void *stream)
+{
+    if (h == nullptr || d_offsets == nullptr || A == nullptr || B == nullptr || sB == nullptr || q == nullptr ||
+        s == nullptr)
+        return MPQ_ERR_NULL;
+    if ((flags & ~(MPQ_POW2 | MPQ_FUSE_QUANT_A)) != 0)
+        return MPQ_ERR_UNSUPPORTED;
+    const bool fuse = (flags & MPQ_FUSE_QUANT_A) != 0;
+    if (fuse ? sA != nullptr : sA == nullptr)
+        return fuse ? MPQ_ERR_UNSUPPORTED : MPQ_ERR_NULL;
+    const int64_t N = 2 * W;
+    if (W <= 0 || W % 128 != 0 || K <= 0 || K % 128 != 0 || lda < K || ldb < K || ldsb < K / 128 || ldq < W)
+        return MPQ_ERR_SHAPE;
+    if (G < 1 || G > 1024 || M_total < 0 || M_total > (int64_t(1) << 31) || K > (int64_t(1) << 31) ||
+        G * N > (int64_t(1) << 31) || lds < M_total || (!fuse && ldsa < M_total) || (H != nullptr && ldh < N))
+        return MPQ_ERR_SHAPE;
+    if (!aligned(A, 16) || (fuse ? lda % 8 != 0 : lda % 16 != 0) || !aligned(B, 16) || ldb % 16 != 0 ||
+        !aligned(q, 16) || ldq % 16 != 0 || !aligned(s, 4) || !aligned(sB, 4) || !aligned(d_offsets, 8) ||
+        (!fuse && !aligned(sA, 4)) || (H != nullptr && (!aligned(H, 16) || ldh % 8 != 0)))
+        return MPQ_ERR_ALIGN;
+    if (M_total == 0)
+        return MPQ_OK;
+    if (mpq_status d = device_ok(h); d != MPQ_OK)
+        return d;
+    mpq::GemmArgs a{};
+    a.M = M_total; a.N = N; a.K = K;
+    a.sB = sB; a.ldsb = ldsb; a.sb_group_stride = (N / 128) * ldsb;
+    a.C = H; a.ldc = ldh;
+    a.offsets = d_offsets; a.G = static_cast<int>(G);
+    a.status = h->d_status; a.timeout_ns = h->timeout_ns;
+    a.sw_q = q; a.sw_ldq = ldq; a.sw_s = s; a.sw_lds = lds;
+    a.sw_width = static_cast<int>(W); a.sw_pow2 = (flags & MPQ_POW2) != 0 ? 1 : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap tmA, tmB;
+    mpq_status e;
+    if ((e = encode_operand(&tmB, B, G * N, K, ldb, 128)) != MPQ_OK)
+        return e;
+    if (fuse) {
+        size_t need = 0;
+        if ((e = mpq_grouped_fused_workspace_bytes(M_total, K, G, &need)) != MPQ_OK)
+            return e;
+        if (h->workspace == nullptr || h->workspace_bytes < need)
+            return MPQ_ERR_WORKSPACE;
+        uint8_t *xq = static_cast<uint8_t *>(h->workspace);
+        float *sx = reinterpret_cast<float *>(xq + align256(static_cast<size_t>(M_total) * static_cast<size_t>(K)));
+        int *ready = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(sx) +
+                                             align256(static_cast<size_t>(K / 128) * static_cast<size_t>(M_total) *
+                                                      sizeof(float)));
+        a.sA = sx; a.ldsa = M_total;
+        mpq::FuseArgs f{};
+        f.x = static_cast<const uint16_t *>(A);
+        f.ldx = lda;
+        f.xq = xq; f.sx = sx; f.ready = ready;
+        f.pow2 = 0;   // the up projection's input: amax/448 scales
+        if ((e = encode_operand(&tmA, xq, M_total, K, K, 128)) != MPQ_OK)
+            return e;
+        return from_cuda(mpq::launch_gemm_swiglu(tmA, tmB, a, false, h->num_sms, st, &f));
+    }
+    a.sA = sA; a.ldsa = ldsa;
+    if ((e = encode_operand(&tmA, static_cast<const uint8_t *>(A), M_total, K, lda, 128)) != MPQ_OK)
+        return e;
+    const bool pair = h->pair_mode == 2 || (h->pair_mode == 1 && M_total >= 2048 * G);
+    return from_cuda(mpq::launch_gemm_swiglu(tmA, tmB, a, pair, h->num_sms, st));
+}
+
 mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
                                         int64_t N, int64_t K, const uint8_t *A, int64_t lda, const float *sA,
                                         int64_t ldsa, const uint8_t *B, int64_t ldb, const float *sB,

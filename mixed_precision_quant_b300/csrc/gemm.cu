@@ -38,6 +38,7 @@
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
 #include "quant_device.cuh"
+#include "swiglu_device.cuh"
 
 namespace mpq {
 namespace {
@@ -75,7 +76,10 @@ struct Cfg {
     static constexpr int BAR_SFULL = BAR_TEMPTY + 2;
     static constexpr int BAR_SEMPTY = BAR_SFULL + SSLOTS;
     static constexpr int BAR_DRAIN = BAR_SEMPTY + SSLOTS;
-    static constexpr int NBARS = BAR_DRAIN + 1;
+    // SwiGLU epilogue: the two promotion warps of a lane quadrant exchange their rows'
+    // half-group max-abs values (one barrier per quadrant, two arrivals)
+    static constexpr int BAR_XCH = BAR_DRAIN + 1;
+    static constexpr int NBARS = BAR_XCH + 4;
     // Register split after the roles diverge (4 x 32 x low + 8 x 32 x high = 168 x 384, the
     // launch's allocation): for dense GEMMs with block B scales the producer, MMA and scale
     // warps run faster with 72 registers (Fprop +4%, Dgrad +1%); the per-column-scale
@@ -180,7 +184,7 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
     }
 }
 
-template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE, bool SK>
+template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE, bool SK, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs p, const FuseArgs f)
@@ -210,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int64_t M = p.M, N = p.N;
     const int KB = static_cast<int>(p.K / BK);
-    const int NT = static_cast<int>((N + BN - 1) / BN);
+    // SwiGLU tiles: 128 output columns, the matching gate and up weight rows side by side
+    const int NT = SWIGLU ? p.sw_width / 128 : static_cast<int>((N + BN - 1) / BN);
+    constexpr int TILE_N = SWIGLU ? 128 : BN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -225,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::BAR_SEMPTY + j), 8);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
+        for (int q = 0; q < 4; ++q)
+            mbar_init(bar(C::BAR_XCH + q), 64);   // every thread of the quadrant's two warps
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             row0 = mt * C::TILE_M;
             rend = static_cast<int>(M);
             ti.g = 0;
-            ti.n0 = nt * BN;
+            ti.n0 = nt * TILE_N;
             ti.brow0 = ti.n0;
             ti.sb_base = 0;
         } else {
@@ -331,13 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = nf ? local % NT : local / mtg, mt = nf ? local / NT : local - nt * mtg;
             row0 = goff[g] + mt * C::TILE_M;
             rend = goff[g + 1];
-            ti.n0 = nt * BN;
+            ti.n0 = nt * TILE_N;
             ti.brow0 = g * static_cast<int>(N) + ti.n0;
             ti.sb_base = static_cast<int64_t>(g) * p.sb_group_stride;
         }
         ti.row0 = row0 + static_cast<int>(rank) * 128;
         ti.row_end = ti.row0 + 128 < rend ? ti.row0 + 128 : rend;
-        ti.brow0 += static_cast<int>(rank) * C::B_ROWS;
+        // pair mode: the odd CTA stages the second half of the tile's B rows (the up weights
+        // of a SwiGLU tile)
+        ti.brow0 += static_cast<int>(rank) * (SWIGLU ? p.sw_width : C::B_ROWS);
         return ti;
     };
 
@@ -371,7 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::STAGE_BYTES);
                         tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, bar(C::BAR_FULL + s), kb * BK, ti.row0);
-                        tma_load_2d(smem_u32(smB + s * C::B_BYTES), &tmB, bar(C::BAR_FULL + s), kb * BK, ti.brow0);
+                        if (SWIGLU) {   // gate rows, then up rows (boxes of 128 rows)
+                            tma_load_2d(smem_u32(smB + s * C::B_BYTES), &tmB, bar(C::BAR_FULL + s), kb * BK, ti.brow0);
+                            tma_load_2d(smem_u32(smB + s * C::B_BYTES + 128 * BK), &tmB, bar(C::BAR_FULL + s), kb * BK,
+                                        ti.brow0 + p.sw_width);
+                        } else {
+                            tma_load_2d(smem_u32(smB + s * C::B_BYTES), &tmB, bar(C::BAR_FULL + s), kb * BK, ti.brow0);
+                        }
                     }
                 }
             }
@@ -462,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             cp_async_4(smem_u32(ssb + j * BN + lane + 32 * i), ok ? sb_row + n : p.sB, ok ? 4u : 0u);
                         }
                     } else if (lane < BN / 128) {
-                        const int nb = ti.n0 / 128 + lane;
+                        // SwiGLU: lane 0 the gate rows' block, lane 1 the up rows'
+                        const int nb = SWIGLU ? (ti.n0 + lane * p.sw_width) / 128 : ti.n0 / 128 + lane;
                         const bool ok = nb * 128 < N;
                         const float *src = SCALE_B == kScaleBlockNK ? sbg + nb * p.ldsb + kb
                                                                     : sbg + static_cast<int64_t>(kb) * p.ldsb + nb;
@@ -482,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tm_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
+        uint32_t xpar = 0;   // SwiGLU epilogue: exchanges done
         Sched sc = sched_init(SK, unit, nunits, T, KB);
         int t, kb0, kb1;
         while (ok && sched_next(sc, t, kb0, kb1)) {
@@ -501,11 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const float sa = ssa[j * 128 + row_in];
-                float sc = 0.0f;
+                float sc = 0.0f, sc2 = 0.0f;
                 if (SCALE_B != kScaleRowKN)
-                    sc = sa * ssb[j * BN + half];
+                    sc = sa * ssb[j * BN + (SWIGLU ? 0 : half)];
+                if (SWIGLU)
+                    sc2 = sa * ssb[j * BN + 1];
+                else
+                    sc2 = sc;
                 const float *sbcol = ssb + j * BN + half * 128;
-                const uint32_t taddr = tmem_base + tm_lane + buf * BN + half * 128;
+                // chunk columns: half * 128 + {0, 32, 64, 96}; SwiGLU: gate half * 64 + {0, 32},
+                // up 128 + half * 64 + {0, 32} (acc[0, 64) gate, acc[64, 128) up, same columns)
+                const uint32_t taddr = tmem_base + tm_lane + buf * BN + (SWIGLU ? half * 64 : half * 128);
+                constexpr uint32_t O2 = SWIGLU ? 128 : 64, O3 = SWIGLU ? 160 : 96;
                 // two TMEM loads in flight: 0,1 | 2 while promoting 0 | 3 while promoting 1
                 uint32_t va[32], vb[32];
                 MPQ_TMEM_LD32(taddr, va);
@@ -513,13 +538,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 MPQ_TMEM_WAIT_LD32(va);
                 MPQ_TMEM_WAIT_LD32(vb);
                 promote_chunk<SCALE_B>(acc, va, 0, sc, sa, sbcol);
-                MPQ_TMEM_LD32(taddr + 64, va);
+                MPQ_TMEM_LD32(taddr + O2, va);
                 promote_chunk<SCALE_B>(acc, vb, 1, sc, sa, sbcol);
-                MPQ_TMEM_LD32(taddr + 96, vb);
+                MPQ_TMEM_LD32(taddr + O3, vb);
                 MPQ_TMEM_WAIT_LD32(va);
-                promote_chunk<SCALE_B>(acc, va, 2, sc, sa, sbcol);
+                promote_chunk<SCALE_B>(acc, va, 2, sc2, sa, sbcol);
                 MPQ_TMEM_WAIT_LD32(vb);
-                promote_chunk<SCALE_B>(acc, vb, 3, sc, sa, sbcol);
+                promote_chunk<SCALE_B>(acc, vb, 3, sc2, sa, sbcol);
                 // Release the partial buffer only after the last FMAs: releasing it as soon as
                 // the loads land lets the next MMAs start earlier and measurably slows the
                 // other warps' TMEM loads (about 25% on 4096 x 18432 x 7168).
@@ -567,6 +592,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], v.z);
                     acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], v.w);
                 }
+            }
+            if (SWIGLU) {
+                // x = silu(gate) * up on the GEMM outputs rounded to BF16 (the values the plain
+                // grouped GEMM writes), then the 1x128 quantization of row m's group of output
+                // columns [n0, n0 + 128), whose other half the quadrant's other warp holds
+                const int m = ti.row0 + quad * 32 + lane;
+                const bool valid = m < ti.row_end;
+                const int c0 = ti.n0 + half * 64;
+                // per 8 columns: round gate and up to BF16, store them when H is kept, and
+                // overwrite the gate accumulators with x (acc[0, 64) then holds x; keeps the
+                // register footprint at the accumulator's)
+                __nv_bfloat16 *crow = p.C != nullptr && valid
+                                          ? static_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(m) * p.ldc
+                                          : nullptr;
+                float amax = 0.0f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t gw[4], uw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int a = c8 * 8 + 2 * k;
+                        const __nv_bfloat162 g2 = __floats2bfloat162_rn(acc[a], acc[a + 1]);
+                        const __nv_bfloat162 u2 = __floats2bfloat162_rn(acc[64 + a], acc[64 + a + 1]);
+                        gw[k] = *reinterpret_cast<const uint32_t *>(&g2);
+                        uw[k] = *reinterpret_cast<const uint32_t *>(&u2);
+                    }
+                    if (crow != nullptr) {   // the cached SwiGLU input (gate | up), BF16
+                        *reinterpret_cast<uint4 *>(crow + c0 + c8 * 8) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+                        *reinterpret_cast<uint4 *>(crow + p.sw_width + c0 + c8 * 8) =
+                            make_uint4(uw[0], uw[1], uw[2], uw[3]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int a = c8 * 8 + 2 * k;
+                        swiglu2(__uint_as_float(bf16x2_lo(gw[k])), __uint_as_float(bf16x2_hi(gw[k])),
+                                __uint_as_float(bf16x2_lo(uw[k])), __uint_as_float(bf16x2_hi(uw[k])), acc[a],
+                                acc[a + 1]);
+                        amax = fmaxf(amax, fmaxf(fabsf(acc[a]), fabsf(acc[a + 1])));
+                    }
+                }
+                // the two half-group max-abs values of each row meet in shared memory (the
+                // output staging area, unused here; two buffers by exchange parity)
+                float *xch = reinterpret_cast<float *>(smO) + (xpar & 1) * 256;
+                xch[half * 128 + quad * 32 + lane] = amax;
+                mbar_arrive(bar(C::BAR_XCH + quad));
+                if (!mbar_wait(bar(C::BAR_XCH + quad), xpar & 1, ctl, 0x04C0 | quad)) {
+                    ok = false;
+                    break;
+                }
+                amax = fmaxf(amax, xch[(1 - half) * 128 + quad * 32 + lane]);
+                ++xpar;
+                const GroupScale gs = make_group_scale(amax, p.sw_pow2 != 0);
+                if (valid) {
+                    uint4 *qd = reinterpret_cast<uint4 *>(p.sw_q + static_cast<int64_t>(m) * p.sw_ldq + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {   // sixteen codes per 16-byte store
+                        uint32_t w[4];
+                        codes_f32<16>(acc + 16 * i, gs, w);
+                        qd[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (half == 0)
+                        p.sw_s[static_cast<int64_t>(ti.n0 / 128) * p.sw_lds + m] = gs.s;
+                }
+                continue;
             }
             // Output: rows [ti.row0 + 32 quad, +32), columns [ti.n0 + 128 half, +128).  A warp
             // whose 32 rows all belong to this tile stages row pieces (128 bytes in pair mode,
@@ -684,11 +773,11 @@ __global__ void wait_selftest_kernel(int *status, uint64_t timeout_ns)
     }
 }
 
-template <int SB, bool F32, bool GR, bool PAIR, bool FUSE, bool SK>
+template <int SB, bool F32, bool GR, bool PAIR, bool FUSE, bool SK, bool SWIGLU = false>
 cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
                        const FuseArgs &f, int grid, cudaStream_t st)
 {
-    auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE, SK>;
+    auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE, SK, SWIGLU>;
     const size_t smem = smem_bytes<PAIR>(GR);
     static std::atomic<uint64_t> configured{0};   // per instantiation: devices already set up
     if (cudaError_t e = ensure_max_dyn_smem(kern, smem, configured); e != cudaSuccess)
@@ -778,6 +867,36 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
 #undef MPQ_G2
 #undef MPQ_G
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_swiglu(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, bool pair,
+                               int num_sms, cudaStream_t st, const FuseArgs *fuse)
+{
+    if (a.offsets == nullptr || a.G > kMaxGroups || a.sw_q == nullptr || a.sw_width <= 0 || a.sw_width % 128 != 0 ||
+        a.N != 2 * static_cast<int64_t>(a.sw_width))
+        return cudaErrorInvalidValue;
+    const int tile_m = pair ? 256 : 128;
+    // upper bound: every expert may add one partial m-tile
+    const int64_t tiles = ((a.M + tile_m - 1) / tile_m + a.G) * (a.sw_width / 128);
+    if (tiles <= 0)
+        return cudaSuccess;
+    // the output view is not used (no TMA stores): tmB stands in for it
+    const FuseArgs none{};
+    if (fuse != nullptr) {   // single-SM tiles, one cooperative CTA per SM
+        if (pair)
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaMemsetAsync(fuse->ready, 0, sizeof(int) * static_cast<size_t>(a.G), st);
+        if (e != cudaSuccess)
+            return e;
+        return launch_one<kScaleBlockNK, false, true, false, true, false, true>(tmA, tmB, tmB, a, *fuse, num_sms, st);
+    }
+    if (pair) {
+        const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
+        return launch_one<kScaleBlockNK, false, true, true, false, false, true>(tmA, tmB, tmB, a, none,
+                                                                               static_cast<int>(2 * (pairs < 1 ? 1 : pairs)), st);
+    }
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    return launch_one<kScaleBlockNK, false, true, false, false, false, true>(tmA, tmB, tmB, a, none, grid, st);
 }
 
 cudaError_t launch_wait_selftest(int *status, uint64_t timeout_ns, cudaStream_t st)

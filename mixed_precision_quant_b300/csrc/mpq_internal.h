@@ -86,6 +86,19 @@ struct GemmArgs {
     // strip of B read once).  Dense GEMMs take the smaller operand as the one re-read;
     // grouped GEMMs decide per expert (n-fastest when its rows outnumber its weight rows).
     int n_fastest;
+    // Fused SwiGLU epilogue (grouped up projection, the input of the down projection): B rows
+    // [0, W) of each expert are the gate weights and [W, 2 W) the up weights (N = 2 W); an
+    // output tile covers columns [n0, n0 + 128) of x = silu(gate) * up, staging gate and up
+    // side by side in the MMA's 256 columns.  Written: the 1x128 quantization of x, codes
+    // sw_q [M][sw_ldq] and scales sw_s [W/128][sw_lds] (power-of-2 scales when sw_pow2), and,
+    // when C is not null, the BF16 gate and up values in C [M][ldc >= 2 W] (the cached
+    // SwiGLU input).
+    uint8_t *sw_q;
+    int64_t sw_ldq;
+    float *sw_s;
+    int64_t sw_lds;
+    int sw_width;
+    int sw_pow2;
 };
 
 // Fused activation quantization: the token rows come as BF16 x [M, K] (ldx elements) and
@@ -114,6 +127,10 @@ struct FuseArgs {
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
                         int scale_b, bool out_fp32, bool pair, int num_sms, cudaStream_t st,
                         const FuseArgs *fuse = nullptr);
+// The grouped GEMM with the SwiGLU epilogue (a.sw_q set): weight block scales, tmB in boxes of
+// 128 rows, tmC unused (the BF16 gate / up values are stored directly when a.C is set).
+cudaError_t launch_gemm_swiglu(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a, bool pair,
+                               int num_sms, cudaStream_t st, const FuseArgs *fuse = nullptr);
 int gemm_b_box_rows(bool pair);
 
 // The same GEMM for power-of-2 scales on the microscaling MMA (kind::mxf8f6f4.block_scale):
