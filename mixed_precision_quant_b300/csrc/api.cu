@@ -545,7 +545,7 @@ mpq_status fp8_gemm_mx_pow2(mpq_handle h, int op, int64_t M, int64_t N, int64_t 
         return st;
     if ((st = encode_operand(&tmB, B, N, K, ldb, 128)) != MPQ_OK)
         return st;
-    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32, true)) != MPQ_OK)
+    if ((st = encode_output(&tmC, C, M, N, ldc, out_dtype == MPQ_OUT_FP32, false)) != MPQ_OK)
         return st;
     mpq::GemmArgs a{};
     a.M = M; a.N = N; a.K = K;

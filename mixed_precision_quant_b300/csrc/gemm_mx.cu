@@ -42,7 +42,7 @@ namespace {
 
 constexpr int BK = 128;
 constexpr int BN = 256;
-constexpr int STAGES = 5;
+constexpr int STAGES = 6;
 constexpr int WRITERS = 4;                      // scale-factor writer warps
 constexpr int kThreads = 512;
 constexpr uint32_t A_BYTES = 128 * BK;          // this CTA's 128 rows of A per slice
@@ -51,7 +51,9 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // accumulator 0..255, scale slots from 256
 constexpr uint32_t SF_COL0 = 256;               // slot j: SFA at 256 + 16 j (4 columns), SFB at +4 (8)
 constexpr uint32_t SF_SLOT_BYTES = 3 * 512;     // shared-memory scale words per slice: SFA, SFB 0-127, SFB 128-255
-constexpr uint32_t STAGE_OUT = 4096;            // output staging: one 4 KB buffer per epilogue warp
+constexpr uint32_t STAGE_OUT = 2048;            // output staging: one 2 KB buffer per epilogue warp
+constexpr int ROWB = STAGE_OUT / 32;            // bytes per staged row piece (64-byte swizzle)
+constexpr int PCS = ROWB / 16;                  // 16-byte pieces per row piece
 constexpr int OUT_BUFS = 1;
 constexpr int kStatusScale = 9;
 
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ncol0 = nt * BN + half * 128;
             if (ncol0 < N && wrow0 < M) {
                 const uint32_t stg0 = smem_u32(smO + ew * OUT_BUFS * STAGE_OUT);
-                constexpr int COLS = 128 / (OUT_F32 ? 4 : 2);   // columns per 128-byte row piece
+                constexpr int COLS = ROWB / (OUT_F32 ? 4 : 2);  // columns per row piece
 #pragma unroll
                 for (int ch = 0; ch < 128 / COLS; ++ch) {
                     const uint32_t stg = stg0 + (ch % OUT_BUFS) * STAGE_OUT;
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_wait_read0();   // the buffer's previous piece has left shared memory
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the row
+                    for (int j = 0; j < PCS; ++j) {   // 16-byte pieces of the row
                         uint4 w;
                         if (OUT_F32) {
                             const int a0 = ch * COLS + j * 4;
@@ -352,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             w = make_uint4(h[0], h[1], h[2], h[3]);
                         }
-                        // 128-byte swizzle: 16-byte piece j of row r at piece j ^ (r & 7)
-                        const uint32_t off = lane * 128 + ((j ^ (lane & 7)) << 4);
+                        // 64-byte swizzle: 16-byte piece j of row r at piece j ^ ((r >> 1) & 3)
+                        const uint32_t off = lane * ROWB + ((j ^ ((lane >> 1) & 3)) << 4);
                         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg + off), "r"(w.x), "r"(w.y),
                                      "r"(w.z), "r"(w.w)
                                      : "memory");

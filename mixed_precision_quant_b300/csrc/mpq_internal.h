@@ -134,7 +134,8 @@ cudaError_t launch_gemm_swiglu(const CUtensorMap &tmA, const CUtensorMap &tmB, c
 int gemm_b_box_rows(bool pair);
 
 // The same GEMM for power-of-2 scales on the microscaling MMA (kind::mxf8f6f4.block_scale):
-// 2-SM pair tiles of 256 x 256, tmA / tmB in boxes of 128 rows, tmC as in pair mode.
+// 2-SM pair tiles of 256 x 256, tmA / tmB in boxes of 128 rows, tmC in boxes of 32 rows x
+// 64 bytes with 64-byte swizzle.
 cudaError_t launch_gemm_mx(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
                            int scale_b, bool out_fp32, int num_sms, cudaStream_t st);
 
