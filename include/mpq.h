@@ -106,9 +106,11 @@ mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
  *   pair tiles: a 2-CTA cluster on two SMs computes a 256 x 256 tile with 2-SM MMAs (each
  *     SM stages its 128 A rows and half of the B rows);
  *   single-SM tiles: one CTA computes a 128 x 256 tile.
- * mode 1 (default): pair tiles for fp8_gemm_blockscaled; for the row-tiled grouped GEMM
- * pair tiles only when the experts average 2048 rows or more (each expert's rows are
- * rounded up to whole tiles, and a 256-row tile wastes more), else single-SM tiles.
+ * mode 1 (default): pair tiles for fp8_gemm_blockscaled; the row-tiled grouped GEMMs
+ * (fp8_grouped_gemm_blockscaled, fp8_grouped_gemm_swiglu_quant) give pair tiles to the
+ * experts with 1024 token rows or more and single-SM tiles to the others (each expert's rows
+ * are rounded up to whole tiles, and a 256-row tile wastes more on a small expert): two
+ * launches on the caller's stream, each computing only its experts' rows.
  * mode 0: single-SM tiles everywhere.  mode 2: pair tiles everywhere.  Other values:
  * MPQ_ERR_UNSUPPORTED.  The tilings give bit-identical results (with stream-K off). */
 mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
@@ -373,9 +375,8 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
  *              (sA must be NULL; needs the handle's workspace; cooperative launch).
  * Rows outside every expert are not written.  The codes, scales and H equal those of
  * fp8_grouped_gemm_blockscaled (BF16 out, same tiling) followed by fp8_swiglu_quant_1x128,
- * bit for bit.  Tiling as for fp8_grouped_gemm_blockscaled's row tiles (pair tiles when the
- * experts average 2048 rows or more under the default mpq_set_gemm_cta_pair mode; single-SM
- * tiles with MPQ_FUSE_QUANT_A).
+ * bit for bit.  Tiling as for fp8_grouped_gemm_blockscaled's row tiles (see
+ * mpq_set_gemm_cta_pair; single-SM tiles with MPQ_FUSE_QUANT_A).
  * Requirements: 1 <= G <= 1024; W % 128 == 0; K % 128 == 0; A, B, q, H 16-byte aligned;
  * lda, ldb, ldq % 16 == 0 (lda % 8 == 0 for BF16 A); ldh % 8 == 0; sA, sB, s 4-byte
  * aligned.  Asynchronous on `stream`; nothing is allocated.

@@ -457,8 +457,9 @@ def mpq_set_wait_timeout(timeout_ns: int, device=None):
 
 def mpq_set_gemm_cta_pair(mode, device=None):
     """Tiling of the row-tiled GEMMs: 1 or True (default) -- 2-SM pair tiles for dense GEMMs,
-    for grouped ones only when experts average 2048 rows or more; 0 or False -- single-SM
-    tiles everywhere; 2 -- pair tiles everywhere."""
+    for grouped ones for the experts with 1024 rows or more (the others on single-SM tiles,
+    in a second launch); 0 or False -- single-SM tiles everywhere; 2 -- pair tiles
+    everywhere."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     _check("mpq_set_gemm_cta_pair", _lib.mpq_set_gemm_cta_pair(_handle(dev), int(mode)))
 

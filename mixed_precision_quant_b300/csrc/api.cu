@@ -253,6 +253,9 @@ mpq_status mpq_set_workspace(mpq_handle h, void *ptr, size_t bytes)
     return MPQ_OK;
 }
 
+// Grouped row tiles: experts with at least this many token rows take 2-SM pair tiles.
+constexpr int64_t kPairExpertRows = 1024;
+
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 mpq_status mpq_grouped_fused_workspace_bytes(int64_t M_total, int64_t K, int64_t G, size_t *bytes)
@@ -742,8 +745,22 @@ mpq_status fp8_grouped_gemm_swiglu_quant(mpq_handle h, int64_t G, const int64_t 
     a.sA = sA; a.ldsa = ldsa;
     if ((e = encode_operand(&tmA, static_cast<const uint8_t *>(A), M_total, K, lda, 128)) != MPQ_OK)
         return e;
-    const bool pair = h->pair_mode == 2 || (h->pair_mode == 1 && M_total >= 2048 * G);
-    return from_cuda(mpq::launch_gemm_swiglu(tmA, tmB, a, pair, h->num_sms, st));
+    // tiling as fp8_grouped_gemm_blockscaled's row tiles (large experts on pair tiles)
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool pair = pass == 0;
+        mpq::GemmArgs ap = a;
+        if (h->pair_mode == 1) {
+            if (pair && M_total < kPairExpertRows)
+                continue;
+            ap.min_rows = pair ? kPairExpertRows : 0;
+            ap.max_rows = pair ? 0x7FFFFFFF : kPairExpertRows;
+        } else if (pair != (h->pair_mode == 2)) {
+            continue;
+        }
+        if ((e = from_cuda(mpq::launch_gemm_swiglu(tmA, tmB, ap, pair, h->num_sms, st))) != MPQ_OK)
+            return e;
+    }
+    return MPQ_OK;
 }
 
 mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *d_offsets, int64_t M_total,
@@ -782,8 +799,9 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     a.C = C; a.ldc = ldc;
     a.offsets = d_offsets; a.G = static_cast<int>(G);
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA;
     if (weight_tiles) {
+        CUtensorMap tmB;
         if ((st = encode_operand(&tmA, A, M_total, K, lda, mpq::decode_x_box_rows())) != MPQ_OK)
             return st;
         if ((st = encode_operand(&tmB, B, G * N, K, ldb, 128)) != MPQ_OK)
@@ -793,17 +811,33 @@ mpq_status fp8_grouped_gemm_blockscaled(mpq_handle h, int64_t G, const int64_t *
     }
     if ((st = encode_operand(&tmA, A, M_total, K, lda, 128)) != MPQ_OK)
         return st;
-    // Pair tiles round every expert's rows up to 256, single-SM tiles to 128: by default the
-    // grouped GEMM takes pairs only for experts of 2048 rows or more on average.
-    const bool pair = h->pair_mode == 2 || (h->pair_mode == 1 && M_total >= 2048 * G);
-    if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
-        return st;
-    CUtensorMap tmC;
-    if ((st = encode_output(&tmC, C, M_total, N, ldc, out_dtype == MPQ_OUT_FP32, pair)) != MPQ_OK)
-        return st;
-    return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, mpq::kScaleBlockNK, out_dtype == MPQ_OUT_FP32, pair,
-                                      h->num_sms,
-                                      static_cast<cudaStream_t>(stream)));
+    // Tiling: pair tiles round an expert's rows up to 256, single-SM tiles up to 128.  By
+    // default experts with kPairExpertRows rows or more take pair tiles (faster per row, little
+    // padding) and the others single-SM tiles, in two launches on the stream, each computing
+    // only its experts' rows; mode 0 / 2: single-SM / pair tiles for every expert.
+    const bool fp32 = out_dtype == MPQ_OUT_FP32;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool pair = pass == 0;
+        mpq::GemmArgs ap = a;
+        if (h->pair_mode == 1) {
+            if (pair && M_total < kPairExpertRows)
+                continue;   // no expert can be that large
+            ap.min_rows = pair ? kPairExpertRows : 0;
+            ap.max_rows = pair ? 0x7FFFFFFF : kPairExpertRows;
+        } else if (pair != (h->pair_mode == 2)) {
+            continue;
+        }
+        CUtensorMap tmB, tmC;
+        if ((st = encode_operand(&tmB, B, G * N, K, ldb, mpq::gemm_b_box_rows(pair))) != MPQ_OK)
+            return st;
+        if ((st = encode_output(&tmC, C, M_total, N, ldc, fp32, pair)) != MPQ_OK)
+            return st;
+        if ((st = from_cuda(mpq::launch_gemm(tmA, tmB, tmC, ap, mpq::kScaleBlockNK, fp32, pair, h->num_sms, cs))) !=
+            MPQ_OK)
+            return st;
+    }
+    return MPQ_OK;
 }
 
 mpq_status mpq_selftest_wait_timeout(mpq_handle h, uint64_t timeout_ns, void *stream)

@@ -250,6 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_relinquish();
         }
     }
+    // m-tiles of an expert with `rows` token rows; experts outside [min_rows, max_rows) belong
+    // to another launch and get none
+    auto expert_mtiles = [&](int rows) -> int {
+        return rows >= p.min_rows && rows < p.max_rows ? (rows + C::TILE_M - 1) / C::TILE_M : 0;
+    };
     if (GROUPED && warp == 2) {
         // Expert schedule: offsets clamped into [0, M] and made monotone (running max),
         // then the exclusive prefix sum of (pair) m-tiles per expert, times the n-tiles.
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e0 = lane * perg, e1 = e0 + perg < G ? e0 + perg : G;
         int cnt = 0;
         for (int g = e0; g < e1; ++g)
-            cnt += static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
+            cnt += expert_mtiles(goff[g + 1] - goff[g]);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ex = incl - cnt;
         for (int g = e0; g < e1; ++g) {
             gtile[g] = ex * NT;
-            ex += static_cast<int>((goff[g + 1] - goff[g] + C::TILE_M - 1) / C::TILE_M);
+            ex += expert_mtiles(goff[g + 1] - goff[g]);
         }
         if (lane == 31)
             gtile[G] = incl * NT;
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ti.g = g;
             const int local = t - gtile[g];
             const int rows_g = goff[g + 1] - goff[g];
-            const int mtg = (rows_g + C::TILE_M - 1) / C::TILE_M;
+            const int mtg = expert_mtiles(rows_g);
             // an expert with more token rows than weight rows reads each row strip once and
             // keeps its (smaller) weight in L2; otherwise each weight strip is read once
             const bool nf = rows_g > N;

@@ -86,6 +86,9 @@ struct GemmArgs {
     // strip of B read once).  Dense GEMMs take the smaller operand as the one re-read;
     // grouped GEMMs decide per expert (n-fastest when its rows outnumber its weight rows).
     int n_fastest;
+    // Grouped GEMMs: only experts with min_rows <= rows < max_rows are computed by this launch
+    // (the others' rows are left to another launch); 0 and INT32_MAX take every expert.
+    int min_rows = 0, max_rows = 0x7FFFFFFF;
     // Fused SwiGLU epilogue (grouped up projection, the input of the down projection): B rows
     // [0, W) of each expert are the gate weights and [W, 2 W) the up weights (N = 2 W); an
     // output tile covers columns [n0, n0 + 128) of x = silu(gate) * up, staging gate and up
