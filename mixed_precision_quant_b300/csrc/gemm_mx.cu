@@ -23,7 +23,7 @@
 //               matrices: row scales, columns 0-127, 128-255).  Four warps keep four
 //               slices' scale loads in flight: one warp would wait out one global-load
 //               latency per slice, longer than the slice's MMAs;
-//   warp 4      TMA producer: E4M3 slices into a 4-stage shared-memory ring;
+//   warp 4      TMA producer: E4M3 slices into a 6-stage shared-memory ring;
 //   warp 5      MMA issuer (even CTA): per slice three tcgen05.cp of the scale words into a
 //               TMEM slot (in order with its MMAs, so no round trip through other warps),
 //               four MMAs (K = 32 each) into one 256-column FP32 accumulator, one commit per
