@@ -16,19 +16,18 @@
 //
 // Design (B300, persistent, 2-CTA clusters computing 256 x 256 tiles with cta_group::2 MMAs,
 // 16 warps per CTA):
-//   warps 0-3   scale-factor writers, warp w for the slices held in stage w: each reads its
-//               slice's 128 row scales of A (this CTA's rows) and 256 column scales of B,
-//               converts them to UE8M0 words and writes them into the stage's slot of a
-//               shared-memory ring in the layout tcgen05.cp takes (three 32-row x 16-byte
-//               matrices: row scales, columns 0-127, 128-255).  Four warps keep four
-//               slices' scale loads in flight: one warp would wait out one global-load
-//               latency per slice, longer than the slice's MMAs;
+//   warps 0-3   scale-factor writers: a slot of scale words covers up to four consecutive
+//               slices of a tile, byte q of each word holding slice q's UE8M0 scale; warp w
+//               takes every fourth slot-group, reads the group's row scales of A (this CTA's
+//               rows) and 256 column scales of B and writes them into a shared-memory ring
+//               in the layout tcgen05.cp takes (three 32-row x 16-byte matrices: row scales,
+//               columns 0-127, 128-255);
 //   warp 4      TMA producer: E4M3 slices into a 6-stage shared-memory ring;
-//   warp 5      MMA issuer (even CTA): per slice three tcgen05.cp of the scale words into a
-//               TMEM slot (in order with its MMAs, so no round trip through other warps),
-//               four MMAs (K = 32 each) into one 256-column FP32 accumulator, one commit per
-//               slice (frees the operand stage and the scale slot in both CTAs) and one per
-//               tile (accumulator complete);
+//   warp 5      MMA issuer (even CTA): once per four slices three tcgen05.cp of a slot into
+//               TMEM (in order with its MMAs); per slice four MMAs (K = 32 each) whose
+//               descriptor selects the slice's byte of the scale words, into one 256-column
+//               FP32 accumulator; one commit per slice (frees the operand stage), one per
+//               group of four (frees the scale slot) and one per tile (accumulator complete);
 //   warps 8-15  epilogue: read the accumulator (32 lanes x 128 columns per warp) into
 //               registers, release it to the MMA issuer (the next tile's MMAs start), then
 //               write BF16 or FP32 through swizzled staging buffers and TMA stores.
@@ -50,7 +49,11 @@ constexpr uint32_t B_BYTES = 128 * BK;          // this CTA's half of the tile's
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;             // accumulator 0..255, scale slots from 256
 constexpr uint32_t SF_COL0 = 256;               // slot j: SFA at 256 + 16 j (4 columns), SFB at +4 (8)
-constexpr uint32_t SF_SLOT_BYTES = 3 * 512;     // shared-memory scale words per slice: SFA, SFB 0-127, SFB 128-255
+constexpr uint32_t SF_SLOT_BYTES = 3 * 512;     // shared-memory scale words per slot: SFA, SFB 0-127, SFB 128-255
+// Scale slots, each holding four slices' scales.  As many as writer warps: warp w fills slot w
+// only, so a warp waiting for its slot's previous group is never two phases of the slot's
+// barriers away from it (the parity waits stay unambiguous).
+constexpr int SF_SLOTS = WRITERS;
 constexpr uint32_t STAGE_OUT = 2048;            // output staging: one 2 KB buffer per epilogue warp
 constexpr int ROWB = STAGE_OUT / 32;            // bytes per staged row piece (64-byte swizzle)
 constexpr int PCS = ROWB / 16;                  // 16-byte pieces per row piece
@@ -60,12 +63,13 @@ constexpr int kStatusScale = 9;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_DONE = BAR_FULL + STAGES;
 constexpr int BAR_SFREADY = BAR_DONE + STAGES;
-constexpr int BAR_ACCFULL = BAR_SFREADY + STAGES;
+constexpr int BAR_SFDONE = BAR_SFREADY + SF_SLOTS;
+constexpr int BAR_ACCFULL = BAR_SFDONE + SF_SLOTS;
 constexpr int BAR_ACCEMPTY = BAR_ACCFULL + 1;
 constexpr int BAR_DRAIN = BAR_ACCEMPTY + 1;
 constexpr int NBARS = BAR_DRAIN + 1;
 
-constexpr size_t kSmem = 1024 + STAGES * STAGE_BYTES + 8 * OUT_BUFS * STAGE_OUT + STAGES * SF_SLOT_BYTES +
+constexpr size_t kSmem = 1024 + STAGES * STAGE_BYTES + 8 * OUT_BUFS * STAGE_OUT + SF_SLOTS * SF_SLOT_BYTES +
                          NBARS * sizeof(uint64_t) + 32;
 
 // Register split after the roles diverge: 8 x 32 x 88 + 8 x 32 x 168 = 65536 = 512 x 128.
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smB = smA + STAGES * A_BYTES;
     uint8_t *smO = smB + STAGES * B_BYTES;
     uint8_t *smSF = smO + 8 * OUT_BUFS * STAGE_OUT;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smSF + STAGES * SF_SLOT_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smSF + SF_SLOTS * SF_SLOT_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
 
@@ -138,7 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(BAR_FULL + s), 1);
             mbar_init(bar(BAR_DONE + s), 1);
-            mbar_init(bar(BAR_SFREADY + s), 2);   // the writer warp of each CTA of the pair
+        }
+        for (int j = 0; j < SF_SLOTS; ++j) {
+            mbar_init(bar(BAR_SFREADY + j), 2);   // the writer warp of each CTA of the pair
+            mbar_init(bar(BAR_SFDONE + j), 1);    // the MMAs that read the slot completed
         }
         mbar_init(bar(BAR_ACCFULL), 1);
         mbar_init(bar(BAR_ACCEMPTY), 16);        // 8 epilogue warps in each CTA
@@ -166,69 +173,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow) : "memory");
         if (warp < 4) {
             // ---------------------------------------------------------- scale-factor writers
-            // Warp w takes the slices held in stage w.  Lane r writes row r of the slot's three
-            // 32-row x 16-byte matrices: the UE8M0
-            // words of A rows r + 32 j, B columns r + 32 j and B columns 128 + r + 32 j
-            // (j = 0..3), each word's four bytes equal.
+            // The scale words of up to four consecutive slices of a tile share one slot: byte q
+            // of each word is the UE8M0 scale of the group's slice q (its MMAs select byte q), so
+            // the MMA issuer copies a slot into TMEM once per four slices.  Lane r writes row r of
+            // the slot's three 32-row x 16-byte matrices: the words of A rows r + 32 j, B
+            // columns r + 32 j and B columns 128 + r + 32 j (j = 0..3).  Warp w takes the groups
+            // gc = w, w + 4, ... of the unit's sequence (slot gc % SF_SLOTS): four warps keep
+            // their groups' scale loads in flight; warp w fills slot w.
             bool bad = false;
-            // this warp's slices are it = warp, warp + 4, ...: position (t, kb) of slice it in
-            // the unit's tile sequence, advanced four slices at a time; the loads of the next
-            // slice are issued before the current one is converted, so two of each warp's
-            // slices (eight per CTA) have their scale loads in flight.  Slice it uses ring
-            // slot it % STAGES.
-            int t = unit, kb = warp;
-            while (kb >= KB && t < T) { kb -= KB; t += nunits; }
-            auto load = [&](int tt, int kk, float (&fa)[4], float (&fb)[8]) {
-                const int mt = p.n_fastest ? tt / NT : tt % MT, nt = p.n_fastest ? tt % NT : tt / MT;
+            const int GPT = (KB + 3) / 4;   // scale groups per tile
+            uint32_t gc = 0;
+            for (int t = unit; t < T; t += nunits) {
+                const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
                 const int64_t row0 = static_cast<int64_t>(mt) * 256 + rank * 128;
-                const float *sa_row = p.sA + static_cast<int64_t>(kk) * p.ldsa;
+                const int64_t n0 = static_cast<int64_t>(nt) * BN;
+                for (int gi = 0; gi < GPT; ++gi, ++gc) {
+                    if ((gc & 3u) != static_cast<uint32_t>(warp))
+                        continue;
+                    const uint32_t slot = gc % SF_SLOTS, ph = (gc / SF_SLOTS) & 1;
+                    float fa[4][4], fb[4][8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {   // rows past M take scale 1 (their products are zero)
-                    const int64_t r = row0 + lane + 32 * j;
-                    fa[j] = r < M ? sa_row[r] : 1.0f;
-                }
-                b_scales<SCALE_B>(p, static_cast<int64_t>(nt) * BN, lane, kk, fb);
-            };
-            float fa[4], fb[8];
-            if (t < T)
-                load(t, kb, fa, fb);
-            for (uint32_t it = warp; t < T; it += WRITERS) {
-                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                int t2 = t, kb2 = kb + WRITERS;
-                while (kb2 >= KB && t2 < T) { kb2 -= KB; t2 += nunits; }
-                float fa2[4], fb2[8];
-                if (t2 < T)
-                    load(t2, kb2, fa2, fb2);
-                // the slot is free once the copies of its previous slice have completed
-                if (!mbar_wait(bar(BAR_DONE + s), ph ^ 1, ctl, 0x0600 | s))
-                    goto writer_done;
-                {
+                    for (int q = 0; q < 4; ++q) {   // slices past the tile's K take scale 1 (unused)
+                        const int kb = gi * 4 + q;
+                        if (kb < KB) {
+                            const float *sa_row = p.sA + static_cast<int64_t>(kb) * p.ldsa;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {   // rows past M: scale 1 (zero products)
+                                const int64_t r = row0 + lane + 32 * j;
+                                fa[q][j] = r < M ? sa_row[r] : 1.0f;
+                            }
+                            b_scales<SCALE_B>(p, n0, lane, kb, fb[q]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                fa[q][j] = 1.0f;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                fb[q][j] = 1.0f;
+                        }
+                    }
                     uint32_t w[12];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        w[j] = ue8m0_of(fa[j], bad) * 0x01010101u;
+                    for (int j = 0; j < 12; ++j)
+                        w[j] = 0;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        w[4 + j] = ue8m0_of(fb[j], bad) * 0x01010101u;
-                    const uint32_t slot = smem_u32(smSF + s * SF_SLOT_BYTES) + lane * 16;
+                    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            w[j] |= ue8m0_of(fa[q][j], bad) << (8 * q);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            w[4 + j] |= ue8m0_of(fb[q][j], bad) << (8 * q);
+                    }
+                    // the slot is free once the MMAs that read its previous group completed
+                    if (!mbar_wait(bar(BAR_SFDONE + slot), ph ^ 1, ctl, 0x0600 | slot))
+                        goto writer_done;
+                    const uint32_t dst = smem_u32(smSF + slot * SF_SLOT_BYTES) + lane * 16;
 #pragma unroll
                     for (int q = 0; q < 3; ++q)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot + q * 512),
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + q * 512),
                                      "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
                                      : "memory");
+                    fence_proxy_async_smem();   // visible to tcgen05.cp
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_remote(mapa_shared(bar(BAR_SFREADY + slot), 0));
                 }
-                fence_proxy_async_smem();   // visible to tcgen05.cp
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_remote(mapa_shared(bar(BAR_SFREADY + s), 0));
-                t = t2;
-                kb = kb2;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    fa[j] = fa2[j];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    fb[j] = fb2[j];
             }
         writer_done:
             if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status != nullptr &&
@@ -266,27 +276,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_mx_e4m3(256, BN);
             const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(smA));
             const uint64_t db0 = sdesc_kmajor_sw128(smem_u32(smB));
-            uint32_t s = 0, ph = 0, tc = 0;
+            uint32_t s = 0, ph = 0, tc = 0, gc = 0;
             for (int t = unit; t < T; t += nunits, ++tc) {
                 if (!mbar_wait(bar(BAR_ACCEMPTY), (tc & 1) ^ 1, ctl, 0x0800))
                     goto mma_done;
                 tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(bar(BAR_SFREADY + s), ph, ctl, 0x0810 | s) ||
-                        !mbar_wait(bar(BAR_FULL + s), ph, ctl, 0x0820 | s))
+                    const uint32_t q = static_cast<uint32_t>(kb & 3);
+                    const uint32_t slot = gc % SF_SLOTS;
+                    const uint32_t sfa = tmem_base + SF_COL0 + 16 * slot;
+                    if (q == 0) {   // a group's first slice: its scale slot into TMEM
+                        if (!mbar_wait(bar(BAR_SFREADY + slot), (gc / SF_SLOTS) & 1, ctl, 0x0810 | slot))
+                            goto mma_done;
+                        tc_fence_after();
+                        const uint32_t sfs = smem_u32(smSF + slot * SF_SLOT_BYTES);
+#pragma unroll
+                        for (int c = 0; c < 3; ++c)   // SFA, SFB 0-127, SFB 128-255: columns +0, +4, +8
+                            tmem_cp_32x128b_x4_pair(sfa + 4 * c, sdesc_rows16(sfs + 512 * c));
+                    }
+                    if (!mbar_wait(bar(BAR_FULL + s), ph, ctl, 0x0820 | s))
                         goto mma_done;
                     tc_fence_after();
                     const uint64_t da = da0 + s * (A_BYTES >> 4), db = db0 + s * (B_BYTES >> 4);
-                    const uint32_t sfa = tmem_base + SF_COL0 + 16 * s;
-                    const uint32_t sfs = smem_u32(smSF + s * SF_SLOT_BYTES);
-#pragma unroll
-                    for (int q = 0; q < 3; ++q)   // SFA, SFB 0-127, SFB 128-255: columns +0, +4, +8
-                        tmem_cp_32x128b_x4_pair(sfa + 4 * q, sdesc_rows16(sfs + 512 * q));
+                    // byte q of every scale word: this slice's scales (B: bits 4-5, A: bits 29-30)
+                    const uint32_t id = idesc | (q << 4) | (q << 29);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        umma_mx_pair(tmem_base, da + 2 * k, db + 2 * k, idesc, sfa, sfa + 4,
-                                     (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_mx_pair(tmem_base, da + 2 * k, db + 2 * k, id, sfa, sfa + 4, (kb > 0 || k > 0) ? 1u : 0u);
                     umma_commit_pair_mc(bar(BAR_DONE + s), 0x3);
+                    if (q == 3 || kb == KB - 1) {   // the group's last slice: its slot may be refilled
+                        umma_commit_pair_mc(bar(BAR_SFDONE + slot), 0x3);
+                        ++gc;
+                    }
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1;
