@@ -276,7 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_mx_e4m3(256, BN);
             const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(smA));
             const uint64_t db0 = sdesc_kmajor_sw128(smem_u32(smB));
+            // a group's scale slot is copied into TMEM during the previous group, so the MMAs
+            // never wait for a copy issued just ahead of them
+            const int GPT = (KB + 3) / 4;
+            const uint32_t ngroups = static_cast<uint32_t>((T - unit + nunits - 1) / nunits) * GPT;
+            auto copy_slot = [&](uint32_t g) -> bool {
+                const uint32_t sl = g % SF_SLOTS;
+                if (!mbar_wait(bar(BAR_SFREADY + sl), (g / SF_SLOTS) & 1, ctl, 0x0810 | sl))
+                    return false;
+                tc_fence_after();
+                const uint32_t sfs = smem_u32(smSF + sl * SF_SLOT_BYTES);
+                const uint32_t dst = tmem_base + SF_COL0 + 16 * sl;
+#pragma unroll
+                for (int c = 0; c < 3; ++c)   // SFA, SFB 0-127, SFB 128-255: columns +0, +4, +8
+                    tmem_cp_32x128b_x4_pair(dst + 4 * c, sdesc_rows16(sfs + 512 * c));
+                return true;
+            };
             uint32_t s = 0, ph = 0, tc = 0, gc = 0;
+            if (ngroups > 0 && !copy_slot(0))
+                goto mma_done;
             for (int t = unit; t < T; t += nunits, ++tc) {
                 if (!mbar_wait(bar(BAR_ACCEMPTY), (tc & 1) ^ 1, ctl, 0x0800))
                     goto mma_done;
@@ -285,15 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t q = static_cast<uint32_t>(kb & 3);
                     const uint32_t slot = gc % SF_SLOTS;
                     const uint32_t sfa = tmem_base + SF_COL0 + 16 * slot;
-                    if (q == 0) {   // a group's first slice: its scale slot into TMEM
-                        if (!mbar_wait(bar(BAR_SFREADY + slot), (gc / SF_SLOTS) & 1, ctl, 0x0810 | slot))
-                            goto mma_done;
-                        tc_fence_after();
-                        const uint32_t sfs = smem_u32(smSF + slot * SF_SLOT_BYTES);
-#pragma unroll
-                        for (int c = 0; c < 3; ++c)   // SFA, SFB 0-127, SFB 128-255: columns +0, +4, +8
-                            tmem_cp_32x128b_x4_pair(sfa + 4 * c, sdesc_rows16(sfs + 512 * c));
-                    }
+                    if (q == 0 && gc + 1 < ngroups && !copy_slot(gc + 1))   // the next group's slot
+                        goto mma_done;
                     if (!mbar_wait(bar(BAR_FULL + s), ph, ctl, 0x0820 | s))
                         goto mma_done;
                     tc_fence_after();
