@@ -185,7 +185,7 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
     for (int i = 0; i < 32; ++i) {
         const float x = __uint_as_float(v[i]);
         if (SCALE_B == kScaleRowKN)
-            acc[c * 32 + i] = __fmaf_rn(__fmul_rn(x, sbcol[c * 32 + i]), sa, acc[c * 32 + i]);
+            acc[c * 32 + i] = __fmaf_rn(x, __fmul_rn(sa, sbcol[c * 32 + i]), acc[c * 32 + i]);
         else
             acc[c * 32 + i] = __fmaf_rn(x, sc, acc[c * 32 + i]);
     }

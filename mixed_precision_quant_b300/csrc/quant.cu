@@ -151,9 +151,10 @@ __device__ __forceinline__ void produce128(uint32_t stage, uint32_t bars, int st
 //
 // One 128-row x 128-column tile per ring slot (four slots); warpgroup h (threads
 // 128h .. +127) takes the CTA's tiles h, h+2, ..., thread rr owning row rr of the tile, with
-// its own staging box and barrier, so the two warpgroups run independently.
+// its own barrier and two staging boxes used in turn, so the two warpgroups run
+// independently and a tile's store drains while the next tile is converted.
 constexpr int QR_STAGES = 4;
-constexpr size_t kRowsSmem = 1024 + QR_STAGES * 2 * kBox + 2 * kBox + (2 * QR_STAGES + 2) * 8 + 16;
+constexpr size_t kRowsSmem = 1024 + QR_STAGES * 2 * kBox + 4 * kBox + (2 * QR_STAGES + 2) * 8 + 16;
 
 template <bool POW2>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -164,9 +165,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad, out_rows = stage + QR_STAGES * 2 * kBox;
-    const uint32_t bars = out_rows + 2 * kBox;          // full[S], empty[S], warpgroup[2]
+    const uint32_t bars = out_rows + 4 * kBox;          // full[S], empty[S], warpgroup[2]
     volatile int *abort_flag =
-        reinterpret_cast<volatile int *>(smem_raw + pad + QR_STAGES * 2 * kBox + 2 * kBox + (2 * QR_STAGES + 2) * 8);
+        reinterpret_cast<volatile int *>(smem_raw + pad + QR_STAGES * 2 * kBox + 4 * kBox + (2 * QR_STAGES + 2) * 8);
     if (threadIdx.x == 0) {
         for (int i = 0; i < QR_STAGES; ++i) {
             mbar_init(bars + 8 * i, 1);
@@ -188,7 +189,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     const int h = t >> 7, rr = t & 127;
     const uint32_t wgbar = bars + 8 * (2 * QR_STAGES + h);
-    const uint32_t out = out_rows + h * kBox;
     const bool elected = rr == 0;
     uint32_t cph = 0;
     uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (!mbar_wait(bars + 8 * st, ph, ctl, 0x1200 | st))
             break;
         const int64_t rb = item / ncb, kb = item - rb * ncb;
+        const uint32_t out = out_rows + (2 * h + ((it >> 1) & 1)) * kBox;   // this tile's staging box
         uint32_t w[64];
         load_row(stage + st * 2 * kBox, rr, w);
         __syncwarp();
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (r < p.rows)
             p.s[kb * p.lds + r] = g.s;
         if (elected)
-            bulk_wait_read0();                 // the previous store has left the staging box
+            bulk_wait_read1();                 // the box's previous store has left it
         if (!wg_sync(wgbar, cph, ctl, 0x1210))
             break;
         write_codes(out, rr, w, g);
@@ -232,20 +233,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // latencies of a pass (shared loads, the max-abs tree, the scale's division).  Here each
 // thread owns half a group -- 64 values -- and the two halves' max-abs values meet in one
 // shuffle, so sixteen consumer warps fit.  Tiles are 128 rows x 128 columns (32 KB of
-// BF16, two 128 x 64 TMA boxes) in a four-stage ring; warpgroup h (warps 8h .. 8h+7) takes
+// BF16, two 128 x 64 TMA boxes) in a three-stage ring; warpgroup h (warps 8h .. 8h+7) takes
 // the CTA's tiles h, h+2, h+4, ..., so the two warpgroups run independently, each with its
-// own staging tiles and barrier.  Within a warpgroup thread u (0..255) holds
+// own barrier and two sets of staging tiles used in turn, so that a tile's code stores drain
+// while the next tile is converted (a fourth input stage does not fit beside them; the
+// second set is worth more: 8192 x 2048 +11%, 8192 x 7168 +4%).  Within a warpgroup thread
+// u (0..255) holds
 //   row pass:    row u/2, columns 64 (u%2) .. +63 (16-byte shared loads);
 //   column pass: lane t of warp wl, for the two columns 16 wl + 8 b + t/4 (b = 0, 1), the
 //                rows 8 rb + 2 (t%4), +1 (rb = 0..15) -- transposing 8x8 matrix loads
 //                (ldmatrix .trans) deliver each as one BF16 pair, 128 bytes per shared
 //                wavefront, so the four lanes of a column hold its 128 values and combine
 //                max-abs values in two shuffles; codes leave as 2-byte shared stores.
-constexpr int QD_STAGES = 4;
+constexpr int QD_STAGES = 3;
 constexpr uint32_t kDualTile = 2 * kBox;          // 128 x 128 BF16
 constexpr int kDualConsumers = 16;
 constexpr int kDualThreads = 32 * (kDualConsumers + 1);
-constexpr size_t kDualSmem = 1024 + QD_STAGES * kDualTile + 4 * kBox + (2 * QD_STAGES + 2) * 8 + 16;
+constexpr size_t kDualSmem = 1024 + QD_STAGES * kDualTile + 8 * kBox + (2 * QD_STAGES + 2) * 8 + 16;
 
 template <bool POW2, bool ROWS>
 __global__ void __launch_bounds__(kDualThreads, 1)
@@ -256,10 +260,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad;
-    const uint32_t out_rows = stage + QD_STAGES * kDualTile, out_cols = out_rows + 2 * kBox;
-    const uint32_t bars = out_cols + 2 * kBox;        // full[S], empty[S], warpgroup[2]
+    const uint32_t out_rows = stage + QD_STAGES * kDualTile, out_cols = out_rows + 4 * kBox;
+    const uint32_t bars = out_cols + 4 * kBox;        // full[S], empty[S], warpgroup[2]
     volatile int *abort_flag =
-        reinterpret_cast<volatile int *>(smem_raw + pad + QD_STAGES * kDualTile + 4 * kBox + (2 * QD_STAGES + 2) * 8);
+        reinterpret_cast<volatile int *>(smem_raw + pad + QD_STAGES * kDualTile + 8 * kBox + (2 * QD_STAGES + 2) * 8);
     if (threadIdx.x == 0) {
         for (int i = 0; i < QD_STAGES; ++i) {
             mbar_init(bars + 8 * i, 1);
@@ -283,7 +287,6 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const int g2 = u >> 1, sub = u & 1;                    // row pass: row and half
     const int wl = u >> 5;                                  // warp within the warpgroup
     const uint32_t wgbar = bars + 8 * (2 * QD_STAGES + h);
-    const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + h * kBox;
     const bool elected = u == 0;
     uint32_t cph = 0;
     uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
@@ -295,8 +298,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         const int64_t rb = item / ncb, cb = item - rb * ncb;
         const uint32_t tile = stage + st * kDualTile;
         const int64_t y = rb * 128;                         // first row of the tile
+        const uint32_t sb = (it >> 1) & 1;                  // this warpgroup's staging set
+        const uint32_t out_r = out_rows + (2 * h + sb) * kBox, out_c = out_cols + (2 * h + sb) * kBox;
         if (elected)
-            bulk_wait_read0();                             // both staging boxes are free
+            bulk_wait_read1();                             // the set's previous stores have read it
         if (!wg_sync(wgbar, cph, ctl, 0x1510))
             break;
         if (ROWS) {
@@ -369,28 +374,35 @@ __global__ void __launch_bounds__(kDualThreads, 1)
 
 // ------------------------------------------------------------------ 128x128 blocks
 //
-// One 128 x 128 block per tile (two 128 x 64 TMA boxes, 32 KB) in a four-stage ring;
-// warpgroup h (warps 4h .. 4h+3) takes the CTA's tiles h, h+2, ..., so the two warpgroups
-// run independently.  Each thread owns one row of the block; the block max comes from warp
-// shuffles and a 4-warp shared reduction.  Transposed codes are gathered column-wise from
-// the row-code staging box.
-constexpr int QB_STAGES = 4;
+// One 128 x 128 block per tile (two 128 x 64 TMA boxes, 32 KB) in a four-stage ring
+// (three when the transposed codes are written too); warpgroup h (warps 4h .. 4h+3) takes
+// the CTA's tiles h, h+2, ..., so the two warpgroups run independently, each with two sets
+// of staging boxes used in turn (a tile's stores drain while the next tile is converted).
+// Each thread owns one row of the block; the block max comes from warp shuffles and a
+// 4-warp shared reduction.  Transposed codes are gathered column-wise from the row-code
+// staging box.
+template <bool TRANS>
+__host__ __device__ constexpr int qb_stages() { return TRANS ? 3 : 4; }
 constexpr uint32_t kBlockTile = 2 * kBox;
 template <bool TRANS>
-constexpr size_t block_smem_bytes() { return 1024 + QB_STAGES * kBlockTile + (TRANS ? 4 : 2) * kBox + (2 * QB_STAGES + 2) * 8 + 16 + 32; }
+constexpr size_t block_smem_bytes()
+{
+    return 1024 + qb_stages<TRANS>() * kBlockTile + (TRANS ? 8 : 4) * kBox + (2 * qb_stages<TRANS>() + 2) * 8 + 16 + 32;
+}
 
 template <bool POW2, bool TRANS>
 __global__ void __launch_bounds__(kQThreads, 1)
     quant_block_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
+    constexpr int QB_STAGES = qb_stages<TRANS>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad;
-    const uint32_t out_rows = stage + QB_STAGES * kBlockTile, out_cols = out_rows + 2 * kBox;
-    const uint32_t bars = out_cols + (TRANS ? 2 * kBox : 0);   // full[S], empty[S], warpgroup[2]
-    uint8_t *tail = smem_raw + pad + QB_STAGES * kBlockTile + (TRANS ? 4 : 2) * kBox + (2 * QB_STAGES + 2) * 8;
+    const uint32_t out_rows = stage + QB_STAGES * kBlockTile, out_cols = out_rows + 4 * kBox;
+    const uint32_t bars = out_cols + (TRANS ? 4 * kBox : 0);   // full[S], empty[S], warpgroup[2]
+    uint8_t *tail = smem_raw + pad + QB_STAGES * kBlockTile + (TRANS ? 8 : 4) * kBox + (2 * QB_STAGES + 2) * 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tail);
     float *red = reinterpret_cast<float *>(tail + 16);          // 8 per-warp partial maxima
     if (threadIdx.x == 0) {
@@ -414,7 +426,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     const int h = t >> 7, rr = t & 127;
     const uint32_t wgbar = bars + 8 * (2 * QB_STAGES + h);
-    const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + h * kBox;
     const bool elected = rr == 0;
     uint32_t cph = 0;
     uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
@@ -425,6 +436,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
         const int64_t rb = item / ncb, cb = item - rb * ncb;
         const int64_t y = rb * 128;                          // first row of the block
+        const uint32_t sb = (it >> 1) & 1;                   // this warpgroup's staging set
+        const uint32_t out_r = out_rows + (2 * h + sb) * kBox, out_c = out_cols + (2 * h + sb) * kBox;
         uint32_t w[64];
         load_row(stage + st * kBlockTile, rr, w);
         __syncwarp();
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (lane == 0)
             red[warp] = a;
         if (elected)
-            bulk_wait_read0();                              // the staging boxes are free
+            bulk_wait_read1();                              // the set's previous stores have read it
         if (!wg_sync(wgbar, cph, ctl, 0x1410))             // block max published
             break;
         a = fmaxf(fmaxf(red[h * 4], red[h * 4 + 1]), fmaxf(red[h * 4 + 2], red[h * 4 + 3]));
