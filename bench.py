@@ -735,7 +735,7 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
 # ------------------------------------------------------------- profiling cases
 
 PROFILE_CASES = ("fprop", "dgrad", "wgrad", "grouped_up", "grouped_up_swiglu", "decode_fused", "decode_fused_swiglu",
-                 "decode_weights", "swiglu", "dual_x", "dual_dy", "block_t", "requant", "rows", "mx_fprop")
+                 "decode_weights", "swiglu", "dual_x", "dual_dy", "block_t", "requant", "rows", "block_w", "mx_fprop")
 
 
 def run_profile(args):
@@ -755,11 +755,16 @@ def run_profile(args):
     u8, f32 = torch.uint8, torch.float32
     # every setup below avoids the profiled kernel, so that ncu's -s <warmup> skips exactly
     # the warm-up launches
-    if case in ("fprop", "rows", "mx_fprop"):
+    if case in ("fprop", "rows", "block_w", "mx_fprop"):
         d = workloads.dense_fprop(device=dev)
         A = d["A"]
         M, K = A.shape
-        if case == "mx_fprop":
+        if case == "block_w":
+            Wd = d["W"]
+            qw = torch.empty(Wd.shape, dtype=u8, device=dev)
+            sw = torch.empty((Wd.shape[0] // 128, Wd.shape[1] // 128), dtype=f32, device=dev)
+            launch = lambda: mpq.fp8_quant_block_128x128(Wd, q=qw, s=sw)
+        elif case == "mx_fprop":
             qa, sa, _, _ = mpq.fp8_quant_tile_1x128(A, pow2=True)
             qb, _, sb = mpq.fp8_quant_block_128x128(d["W"], pow2=True)
             del d["W"]

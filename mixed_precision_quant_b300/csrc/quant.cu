@@ -233,23 +233,26 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // latencies of a pass (shared loads, the max-abs tree, the scale's division).  Here each
 // thread owns half a group -- 64 values -- and the two halves' max-abs values meet in one
 // shuffle, so sixteen consumer warps fit.  Tiles are 128 rows x 128 columns (32 KB of
-// BF16, two 128 x 64 TMA boxes) in a three-stage ring; warpgroup h (warps 8h .. 8h+7) takes
-// the CTA's tiles h, h+2, h+4, ..., so the two warpgroups run independently, each with its
-// own barrier and two sets of staging tiles used in turn, so that a tile's code stores drain
-// while the next tile is converted (a fourth input stage does not fit beside them; the
-// second set is worth more: 8192 x 2048 +11%, 8192 x 7168 +4%).  Within a warpgroup thread
-// u (0..255) holds
+// BF16, two 128 x 64 TMA boxes) in a four-stage ring; warpgroup h (warps 8h .. 8h+7) takes
+// the CTA's tiles h, h+2, h+4, ..., so the two warpgroups run independently.  The stage count
+// is even so that every stage belongs to one warpgroup: with an odd count a warpgroup could
+// wait on a stage two phases ahead of its barrier, and a parity wait cannot tell those apart.
+// Each warpgroup has its own barrier, one row-code staging tile and two transposed-code
+// staging tiles used in turn; the row codes' store is committed as its own group ahead of
+// the transposed codes', so a tile waits only for the previous tile's row store while the
+// transposed store drains (8192 x 7168 +5% over one staging set).  Within a warpgroup
+// thread u (0..255) holds
 //   row pass:    row u/2, columns 64 (u%2) .. +63 (16-byte shared loads);
 //   column pass: lane t of warp wl, for the two columns 16 wl + 8 b + t/4 (b = 0, 1), the
 //                rows 8 rb + 2 (t%4), +1 (rb = 0..15) -- transposing 8x8 matrix loads
 //                (ldmatrix .trans) deliver each as one BF16 pair, 128 bytes per shared
 //                wavefront, so the four lanes of a column hold its 128 values and combine
 //                max-abs values in two shuffles; codes leave as 2-byte shared stores.
-constexpr int QD_STAGES = 3;
+constexpr int QD_STAGES = 4;
 constexpr uint32_t kDualTile = 2 * kBox;          // 128 x 128 BF16
 constexpr int kDualConsumers = 16;
 constexpr int kDualThreads = 32 * (kDualConsumers + 1);
-constexpr size_t kDualSmem = 1024 + QD_STAGES * kDualTile + 8 * kBox + (2 * QD_STAGES + 2) * 8 + 16;
+constexpr size_t kDualSmem = 1024 + QD_STAGES * kDualTile + 6 * kBox + (2 * QD_STAGES + 2) * 8 + 16;
 
 template <bool POW2, bool ROWS>
 __global__ void __launch_bounds__(kDualThreads, 1)
@@ -260,10 +263,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad;
-    const uint32_t out_rows = stage + QD_STAGES * kDualTile, out_cols = out_rows + 4 * kBox;
+    const uint32_t out_rows = stage + QD_STAGES * kDualTile, out_cols = out_rows + 2 * kBox;
     const uint32_t bars = out_cols + 4 * kBox;        // full[S], empty[S], warpgroup[2]
     volatile int *abort_flag =
-        reinterpret_cast<volatile int *>(smem_raw + pad + QD_STAGES * kDualTile + 8 * kBox + (2 * QD_STAGES + 2) * 8);
+        reinterpret_cast<volatile int *>(smem_raw + pad + QD_STAGES * kDualTile + 6 * kBox + (2 * QD_STAGES + 2) * 8);
     if (threadIdx.x == 0) {
         for (int i = 0; i < QD_STAGES; ++i) {
             mbar_init(bars + 8 * i, 1);
@@ -299,9 +302,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         const uint32_t tile = stage + st * kDualTile;
         const int64_t y = rb * 128;                         // first row of the tile
         const uint32_t sb = (it >> 1) & 1;                  // this warpgroup's staging set
-        const uint32_t out_r = out_rows + (2 * h + sb) * kBox, out_c = out_cols + (2 * h + sb) * kBox;
+        const uint32_t out_r = out_rows + h * kBox, out_c = out_cols + (2 * h + sb) * kBox;
         if (elected)
-            bulk_wait_read1();                             // the set's previous stores have read it
+            bulk_wait_read1();                             // all but the newest group (the last transposed store) are read
         if (!wg_sync(wgbar, cph, ctl, 0x1510))
             break;
         if (ROWS) {
@@ -362,8 +365,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (!wg_sync(wgbar, cph, ctl, 0x1511))
             break;
         if (elected) {
-            if (ROWS)
+            if (ROWS) {
                 tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
+                bulk_commit();
+            }
             tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
             bulk_commit();
         }
@@ -374,20 +379,22 @@ __global__ void __launch_bounds__(kDualThreads, 1)
 
 // ------------------------------------------------------------------ 128x128 blocks
 //
-// One 128 x 128 block per tile (two 128 x 64 TMA boxes, 32 KB) in a four-stage ring
-// (three when the transposed codes are written too); warpgroup h (warps 4h .. 4h+3) takes
-// the CTA's tiles h, h+2, ..., so the two warpgroups run independently, each with two sets
-// of staging boxes used in turn (a tile's stores drain while the next tile is converted).
+// One 128 x 128 block per tile (two 128 x 64 TMA boxes, 32 KB) in a four-stage ring (even:
+// each stage belongs to one warpgroup); warpgroup h (warps 4h .. 4h+3) takes the CTA's tiles
+// h, h+2, ..., so the two warpgroups run independently.  Staging per warpgroup: two row-code
+// boxes used in turn, or, when the transposed codes are written too, one row-code box and
+// two transposed-code boxes, the row store committed as its own group first (a tile then
+// waits only for the previous tile's row store; 2048 x 7168 +9%).
 // Each thread owns one row of the block; the block max comes from warp shuffles and a
 // 4-warp shared reduction.  Transposed codes are gathered column-wise from the row-code
 // staging box.
 template <bool TRANS>
-__host__ __device__ constexpr int qb_stages() { return TRANS ? 3 : 4; }
+__host__ __device__ constexpr int qb_stages() { return 4; }   // even: one owner warpgroup per stage
 constexpr uint32_t kBlockTile = 2 * kBox;
 template <bool TRANS>
 constexpr size_t block_smem_bytes()
 {
-    return 1024 + qb_stages<TRANS>() * kBlockTile + (TRANS ? 8 : 4) * kBox + (2 * qb_stages<TRANS>() + 2) * 8 + 16 + 32;
+    return 1024 + qb_stages<TRANS>() * kBlockTile + (TRANS ? 6 : 4) * kBox + (2 * qb_stages<TRANS>() + 2) * 8 + 16 + 32;
 }
 
 template <bool POW2, bool TRANS>
@@ -400,9 +407,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
     const uint32_t stage = base0 + pad;
-    const uint32_t out_rows = stage + QB_STAGES * kBlockTile, out_cols = out_rows + 4 * kBox;
+    const uint32_t out_rows = stage + QB_STAGES * kBlockTile, out_cols = out_rows + (TRANS ? 2 : 4) * kBox;
     const uint32_t bars = out_cols + (TRANS ? 4 * kBox : 0);   // full[S], empty[S], warpgroup[2]
-    uint8_t *tail = smem_raw + pad + QB_STAGES * kBlockTile + (TRANS ? 8 : 4) * kBox + (2 * QB_STAGES + 2) * 8;
+    uint8_t *tail = smem_raw + pad + QB_STAGES * kBlockTile + (TRANS ? 6 : 4) * kBox + (2 * QB_STAGES + 2) * 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tail);
     float *red = reinterpret_cast<float *>(tail + 16);          // 8 per-warp partial maxima
     if (threadIdx.x == 0) {
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const int64_t rb = item / ncb, cb = item - rb * ncb;
         const int64_t y = rb * 128;                          // first row of the block
         const uint32_t sb = (it >> 1) & 1;                   // this warpgroup's staging set
-        const uint32_t out_r = out_rows + (2 * h + sb) * kBox, out_c = out_cols + (2 * h + sb) * kBox;
+        const uint32_t out_r = out_rows + (TRANS ? h : 2 * h + sb) * kBox, out_c = out_cols + (2 * h + sb) * kBox;
         uint32_t w[64];
         load_row(stage + st * kBlockTile, rr, w);
         __syncwarp();
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (lane == 0)
             red[warp] = a;
         if (elected)
-            bulk_wait_read1();                              // the set's previous stores have read it
+            bulk_wait_read1();                              // all but the newest store group are read
         if (!wg_sync(wgbar, cph, ctl, 0x1410))             // block max published
             break;
         a = fmaxf(fmaxf(red[h * 4], red[h * 4 + 1]), fmaxf(red[h * 4 + 2], red[h * 4 + 3]));
@@ -480,9 +487,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
         if (elected) {
             tma_store_2d(&tmq, out_r, static_cast<int32_t>(cb * 128), static_cast<int32_t>(y));
-            if (TRANS)
-                tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
             bulk_commit();
+            if (TRANS) {
+                tma_store_2d(&tmqT, out_c, static_cast<int32_t>(y), static_cast<int32_t>(cb * 128));
+                bulk_commit();
+            }
         }
     }
     if (elected)
