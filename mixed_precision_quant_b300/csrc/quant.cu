@@ -154,6 +154,7 @@ __device__ __forceinline__ void produce128(uint32_t stage, uint32_t bars, int st
 // its own barrier and two staging boxes used in turn, so the two warpgroups run
 // independently and a tile's store drains while the next tile is converted.
 constexpr int QR_STAGES = 4;
+static_assert(QR_STAGES % 2 == 0, "a stage must belong to one of the two warpgroups");
 constexpr size_t kRowsSmem = 1024 + QR_STAGES * 2 * kBox + 4 * kBox + (2 * QR_STAGES + 2) * 8 + 16;
 
 template <bool POW2>
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 //                wavefront, so the four lanes of a column hold its 128 values and combine
 //                max-abs values in two shuffles; codes leave as 2-byte shared stores.
 constexpr int QD_STAGES = 4;
+static_assert(QD_STAGES % 2 == 0, "a stage must belong to one of the two warpgroups");
 constexpr uint32_t kDualTile = 2 * kBox;          // 128 x 128 BF16
 constexpr int kDualConsumers = 16;
 constexpr int kDualThreads = 32 * (kDualConsumers + 1);
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                        const __grid_constant__ CUtensorMap tmqT, const QuantArgs p)
 {
     constexpr int QB_STAGES = qb_stages<TRANS>();
+    static_assert(QB_STAGES % 2 == 0, "a stage must belong to one of the two warpgroups");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base0 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base0 & 1023u)) & 1023u;
