@@ -133,7 +133,8 @@ def src_digest(files):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ["mixed_precision_quant_b300/csrc/gemm.cu", "mixed_precision_quant_b300/csrc/mpq_device.cuh"]
+GEMM_SOURCES = ["mixed_precision_quant_b300/csrc/gemm.cu", "mixed_precision_quant_b300/csrc/mpq_device.cuh",
+                "mixed_precision_quant_b300/csrc/sched_device.cuh"]
 
 
 def profiled_traffic(name: str, digest: str):

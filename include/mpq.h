@@ -115,8 +115,8 @@ mpq_status mpq_set_wait_timeout(mpq_handle h, uint64_t timeout_ns);
  * MPQ_ERR_UNSUPPORTED.  The tilings give bit-identical results (with stream-K off). */
 mpq_status mpq_set_gemm_cta_pair(mpq_handle h, int enable);
 
-/* Schedule of fp8_gemm_blockscaled through this handle (a throughput choice; the pages'
- * method is the same).  Data-parallel: each CTA (pair) takes whole output tiles.  Stream-K:
+/* Schedule of fp8_gemm_blockscaled and fp8_gemm_mx_pow2 through this handle (a throughput
+ * choice; the pages' method is the same).  Data-parallel: each CTA (pair) takes whole output tiles.  Stream-K:
  * the 128-K slices of all tiles are split evenly over the CTAs (pairs); a tile shared by
  * two of them is finished by the one holding its first slices, which adds the other's
  * partial sum (FP32, through the handle's handover area) before the store, so the last
@@ -287,8 +287,9 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
  *   value is at least 2^-119 (smaller nonzero groups get smaller scales).  The kernel checks
  *   each scale; one that is not representable records MPQ_ERR_SCALE in the handle's status
  *   word (mpq_check_device_status) and the output of that call is not valid.
- * Tiling: 2-SM pair tiles of 256 x 256 (mpq_set_gemm_cta_pair does not apply), a
- * data-parallel schedule (mpq_set_gemm_stream_k does not apply).  Results agree with
+ * Tiling: 2-SM pair tiles of 256 x 256 (mpq_set_gemm_cta_pair does not apply); the
+ * schedule follows mpq_set_gemm_stream_k as fp8_gemm_blockscaled does (stream-K when the
+ * last wave of tiles would be short), sharing the handle's handover area.  Results agree with
  * fp8_gemm_blockscaled within the GEMM tolerance of the method, not bit for bit (the FP32
  * sums are rounded in another order).  Asynchronous on `stream`; nothing is allocated.
  */

@@ -456,6 +456,34 @@ static mpq_status check_gemm_common(int64_t N, int64_t K, const uint8_t *A, int6
     return MPQ_OK;
 }
 
+// Stream-K for a dense GEMM of `tiles` output tiles on `units` CTAs (or CTA pairs): when the
+// tiles fill more than one wave and, in the default mode, the last wave would leave more
+// than a tenth of the machine's time idle, the launch gets the handle's handover area and a
+// new epoch (a->sk_part stays null otherwise).
+static mpq_status setup_stream_k(mpq_handle h, int64_t tiles, int64_t units, mpq::GemmArgs *a, void *stream)
+{
+    bool sk = false;
+    if (h->sk_mode != 0 && tiles > units) {
+        const int64_t waves = (tiles + units - 1) / units;
+        sk = h->sk_mode == 2 || 10 * (waves * units - tiles) > waves * units;
+    }
+    if (!sk)
+        return MPQ_OK;
+    // The flags hold the epoch of the launch that last wrote them; a waiter accepts a flag
+    // >= its own epoch.  Before the counter would overflow, the flags are cleared (in stream
+    // order, ahead of the launch) and the count restarts.
+    if (h->sk_epoch == INT32_MAX) {
+        if (cudaMemsetAsync(h->d_sk_flags, 0, static_cast<size_t>(h->num_sms) * 8 * sizeof(int),
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return MPQ_ERR_CUDA;
+        h->sk_epoch = 0;
+    }
+    a->sk_part = h->d_sk_part;
+    a->sk_flags = h->d_sk_flags;
+    a->sk_epoch = ++h->sk_epoch;
+    return MPQ_OK;
+}
+
 mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int64_t K, const uint8_t *A,
                                 int64_t lda, const float *sA, int64_t ldsa, const uint8_t *B, int64_t ldb,
                                 const float *sB, int64_t ldsb, void *C, int64_t ldc, int out_dtype,
@@ -495,30 +523,10 @@ mpq_status fp8_gemm_blockscaled(mpq_handle h, int op, int64_t M, int64_t N, int6
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
     a.n_fastest = N < M ? 1 : 0;   // re-read the smaller operand (from L2)
-    // Stream-K when the tiles fill more than one wave of CTAs (pairs) and, in the default
-    // mode, the last wave would leave more than a tenth of the machine's time idle.
     const int64_t tile_m = pair ? 256 : 128;
     const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + 255) / 256);
-    const int64_t units = pair ? h->num_sms / 2 : h->num_sms;
-    bool sk = false;
-    if (h->sk_mode != 0 && tiles > units) {
-        const int64_t waves = (tiles + units - 1) / units;
-        sk = h->sk_mode == 2 || 10 * (waves * units - tiles) > waves * units;
-    }
-    if (sk) {
-        // The flags hold the epoch of the launch that last wrote them; a waiter accepts a
-        // flag >= its own epoch.  Before the counter would overflow, the flags are cleared
-        // (in stream order, ahead of the launch) and the count restarts.
-        if (h->sk_epoch == INT32_MAX) {
-            if (cudaMemsetAsync(h->d_sk_flags, 0, static_cast<size_t>(h->num_sms) * 8 * sizeof(int),
-                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
-                return MPQ_ERR_CUDA;
-            h->sk_epoch = 0;
-        }
-        a.sk_part = h->d_sk_part;
-        a.sk_flags = h->d_sk_flags;
-        a.sk_epoch = ++h->sk_epoch;
-    }
+    if ((st = setup_stream_k(h, tiles, pair ? h->num_sms / 2 : h->num_sms, &a, stream)) != MPQ_OK)
+        return st;
     return from_cuda(mpq::launch_gemm(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, pair, h->num_sms,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -559,6 +567,9 @@ mpq_status fp8_gemm_mx_pow2(mpq_handle h, int op, int64_t M, int64_t N, int64_t 
     a.status = h->d_status; a.timeout_ns = h->timeout_ns;
     const int sb = op == MPQ_OP_FPROP ? mpq::kScaleBlockNK : op == MPQ_OP_DGRAD ? mpq::kScaleBlockKN : mpq::kScaleRowKN;
     a.n_fastest = N < M ? 1 : 0;   // re-read the smaller operand (from L2)
+    // 256 x 256 pair tiles; stream-K under the same rule as fp8_gemm_blockscaled
+    if ((st = setup_stream_k(h, ((M + 255) / 256) * ((N + 255) / 256), h->num_sms / 2, &a, stream)) != MPQ_OK)
+        return st;
     return from_cuda(mpq::launch_gemm_mx(tmA, tmB, tmC, a, sb, out_dtype == MPQ_OUT_FP32, h->num_sms,
                                          static_cast<cudaStream_t>(stream)));
 }

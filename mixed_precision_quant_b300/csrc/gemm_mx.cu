@@ -35,6 +35,8 @@
 // MPQ_ERR_SCALE in the status word.
 #include "mpq_internal.h"
 #include "mpq_device.cuh"
+#include "quant_device.cuh"
+#include "sched_device.cuh"
 
 namespace mpq {
 namespace {
@@ -111,7 +113,7 @@ __device__ __forceinline__ void b_scales(const GemmArgs &p, int64_t n0, int lane
         fb[j] = j < 4 ? b0 : b1;
 }
 
-template <int SCALE_B, bool OUT_F32>
+template <int SCALE_B, bool OUT_F32, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs p)
@@ -181,13 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // gc = w, w + 4, ... of the unit's sequence (slot gc % SF_SLOTS): four warps keep
             // their groups' scale loads in flight; warp w fills slot w.
             bool bad = false;
-            const int GPT = (KB + 3) / 4;   // scale groups per tile
             uint32_t gc = 0;
-            for (int t = unit; t < T; t += nunits) {
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
                 const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
                 const int64_t row0 = static_cast<int64_t>(mt) * 256 + rank * 128;
                 const int64_t n0 = static_cast<int64_t>(nt) * BN;
-                for (int gi = 0; gi < GPT; ++gi, ++gc) {
+                // the segment's groups of four slices (a stream-K segment may start or end
+                // inside one; the group's other slices are written too and not used)
+                for (int gi = kb0 >> 2; gi <= (kb1 - 1) >> 2; ++gi, ++gc) {
                     if ((gc & 3u) != static_cast<uint32_t>(warp))
                         continue;
                     const uint32_t slot = gc % SF_SLOTS, ph = (gc / SF_SLOTS) & 1;
@@ -247,11 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 4 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
             uint32_t it = 0;
-            for (int t = unit; t < T; t += nunits) {
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
                 const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
                 const int row0 = mt * 256 + static_cast<int>(rank) * 128;
                 const int brow0 = nt * BN + static_cast<int>(rank) * 128;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(bar(BAR_DONE + s), ph ^ 1, ctl, 0x0700 | s))
                         goto producer_done;
@@ -277,9 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(smA));
             const uint64_t db0 = sdesc_kmajor_sw128(smem_u32(smB));
             // a group's scale slot is copied into TMEM during the previous group, so the MMAs
-            // never wait for a copy issued just ahead of them
-            const int GPT = (KB + 3) / 4;
-            const uint32_t ngroups = static_cast<uint32_t>((T - unit + nunits - 1) / nunits) * GPT;
+            // never wait for a copy issued just ahead of them; the groups of all the unit's
+            // segments, counted as the writers count them
+            uint32_t ngroups = 0;
+            {
+                Sched sc = sched_init(SK, unit, nunits, T, KB);
+                int t, kb0, kb1;
+                while (sched_next(sc, t, kb0, kb1))
+                    ngroups += static_cast<uint32_t>(((kb1 - 1) >> 2) - (kb0 >> 2) + 1);
+            }
             auto copy_slot = [&](uint32_t g) -> bool {
                 const uint32_t sl = g % SF_SLOTS;
                 if (!mbar_wait(bar(BAR_SFREADY + sl), (g / SF_SLOTS) & 1, ctl, 0x0810 | sl))
@@ -295,15 +308,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t s = 0, ph = 0, tc = 0, gc = 0;
             if (ngroups > 0 && !copy_slot(0))
                 goto mma_done;
-            for (int t = unit; t < T; t += nunits, ++tc) {
+            for (Sched sc = sched_init(SK, unit, nunits, T, KB); ;) {
+                int t, kb0, kb1;
+                if (!sched_next(sc, t, kb0, kb1))
+                    break;
                 if (!mbar_wait(bar(BAR_ACCEMPTY), (tc & 1) ^ 1, ctl, 0x0800))
                     goto mma_done;
                 tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     const uint32_t q = static_cast<uint32_t>(kb & 3);
                     const uint32_t slot = gc % SF_SLOTS;
                     const uint32_t sfa = tmem_base + SF_COL0 + 16 * slot;
-                    if (q == 0 && gc + 1 < ngroups && !copy_slot(gc + 1))   // the next group's slot
+                    // a group's first slice (of the segment): copy the next group's slot
+                    if ((q == 0 || kb == kb0) && gc + 1 < ngroups && !copy_slot(gc + 1))
                         goto mma_done;
                     if (!mbar_wait(bar(BAR_FULL + s), ph, ctl, 0x0820 | s))
                         goto mma_done;
@@ -313,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t id = idesc | (q << 4) | (q << 29);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        umma_mx_pair(tmem_base, da + 2 * k, db + 2 * k, id, sfa, sfa + 4, (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_mx_pair(tmem_base, da + 2 * k, db + 2 * k, id, sfa, sfa + 4, (kb > kb0 || k > 0) ? 1u : 0u);
                     umma_commit_pair_mc(bar(BAR_DONE + s), 0x3);
-                    if (q == 3 || kb == KB - 1) {   // the group's last slice: its slot may be refilled
+                    if (q == 3 || kb == kb1 - 1) {   // the group's last slice: its slot may be refilled
                         umma_commit_pair_mc(bar(BAR_SFDONE + slot), 0x3);
                         ++gc;
                     }
@@ -325,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 umma_commit_pair_mc(bar(BAR_ACCFULL), 0x3);
+                ++tc;
             }
         mma_done:
             umma_commit_pair_mc(bar(BAR_DRAIN), 0x1);
@@ -336,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 8, quad = warp & 3, half = ew >> 2;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
         uint32_t tc = 0;
-        for (int t = unit; t < T; t += nunits, ++tc) {
+        Sched sc = sched_init(SK, unit, nunits, T, KB);
+        int t, kb0, kb1;
+        for (; sched_next(sc, t, kb0, kb1); ++tc) {
             const int mt = p.n_fastest ? t / NT : t % MT, nt = p.n_fastest ? t % NT : t / MT;
             if (!mbar_wait_sleepy(bar(BAR_ACCFULL), tc & 1, ctl, 0x0900))
                 break;
@@ -357,6 +377,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_remote(mapa_shared(bar(BAR_ACCEMPTY), 0));   // the next tile's MMAs may start
+            if (SK && kb0 > 0) {
+                // Tail of a tile the previous unit finishes: hand this warp's partial over
+                // (layout [unit][rank][warp][i][lane], coalesced) and announce it.
+                float4 *dst = p.sk_part + ((static_cast<int64_t>(unit) * 2 + rank) * 8 + ew) * 1024 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    dst[32 * i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                              __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p.sk_flags + (unit * 2 + rank) * 8 + ew),
+                                 "r"(p.sk_epoch)
+                                 : "memory");
+                continue;
+            }
+            if (SK && kb1 < KB) {
+                // Head of a tile: add the tail the next unit computed (final sum: head + tail).
+                const int slot = ((unit + 1) * 2 + static_cast<int>(rank)) * 8 + ew;
+                if (!wait_count(p.sk_flags + slot, p.sk_epoch, ctl, 0x0980))
+                    break;
+                const float4 *src = p.sk_part + static_cast<int64_t>(slot) * 1024 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float4 w4 = __ldcg(src + 32 * i);
+                    v[4 * i] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * i]), w4.x));
+                    v[4 * i + 1] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * i + 1]), w4.y));
+                    v[4 * i + 2] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * i + 2]), w4.z));
+                    v[4 * i + 3] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * i + 3]), w4.w));
+                }
+            }
             // rows [row0 + 32 quad, +32), columns [n0 + 128 half, +128) of this CTA's half tile
             const int wrow0 = mt * 256 + static_cast<int>(rank) * 128 + quad * 32;
             const int ncol0 = nt * BN + half * 128;
@@ -414,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int SB, bool F32>
+template <int SB, bool F32, bool SK>
 cudaError_t launch_mx_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &a,
                           int grid, cudaStream_t st)
 {
-    auto kern = gemm_mx_kernel<SB, F32>;
+    auto kern = gemm_mx_kernel<SB, F32, SK>;
     static std::atomic<uint64_t> configured{0};
     if (cudaError_t e = ensure_max_dyn_smem(kern, kSmem, configured); e != cudaSuccess)
         return e;
@@ -447,9 +498,13 @@ cudaError_t launch_gemm_mx(const CUtensorMap &tmA, const CUtensorMap &tmB, const
         return cudaSuccess;
     const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
     const int grid = static_cast<int>(2 * (pairs < 1 ? 1 : pairs));
-#define MPQ_MX(SB, F32)                          \
-    if (scale_b == SB && out_fp32 == F32)        \
-        return launch_mx_one<SB, F32>(tmA, tmB, tmC, a, grid, st);
+    const bool sk = a.sk_part != nullptr;
+    if (sk && tiles < grid / 2)   // stream-K: at least one tile per pair
+        return cudaErrorInvalidValue;
+#define MPQ_MX(SB, F32)                                                                   \
+    if (scale_b == SB && out_fp32 == F32)                                                 \
+        return sk ? launch_mx_one<SB, F32, true>(tmA, tmB, tmC, a, grid, st)              \
+                  : launch_mx_one<SB, F32, false>(tmA, tmB, tmC, a, grid, st);
     MPQ_MX(kScaleBlockNK, false)
     MPQ_MX(kScaleBlockNK, true)
     MPQ_MX(kScaleBlockKN, false)

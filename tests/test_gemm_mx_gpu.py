@@ -109,6 +109,58 @@ def test_mx_wgrad(mpq, T, Kin, Nout):
     assert_gemm_close(_host(C), ref, absref, "mx wgrad")
 
 
+@pytest.mark.parametrize("op,M", [("fprop", 2560), ("wgrad", 2560), ("fprop", 2600), ("dgrad", 2560)])
+def test_mx_stream_k(mpq, op, M):
+    """Stream-K forced on M x 2048 outputs with K = 1280 (2560 rows: 80 pair tiles over 74
+    SM pairs, so nearly every tile is split between two units, and the runs start and end
+    inside groups of four slices; 2600 rows add a ragged last row of tiles).  Every output is
+    within FP32 rounding of the data-parallel schedule's (head + tail instead of one
+    accumulation: a dropped, doubled or misplaced partial would not be); two runs agree bit
+    for bit; sampled outputs meet the oracle bound."""
+    N, K = 2048, 1280
+    g = torch.Generator().manual_seed(31)
+    if op == "fprop":
+        a = _bf16((M, K), 1.0, 32, outliers=0.01)
+        w = _bf16((N, K), 0.02, 33)
+        qa, sa = oracle.quant_tile_1x128(bf16_bits(a), pow2=True)
+        qb, _, sb = oracle.quant_block_128x128(bf16_bits(w), pow2=True)
+        o, mop = oracle.FPROP, mpq.FPROP
+    elif op == "dgrad":   # dX [M, N] = dY [M, K] W_lin [K, N]: B = W_lin^T codes, [K/128][N/128] scales
+        dy = workloads.student_t3((M, K), 1e-3, g, "cpu")
+        w = _bf16((K, N), 0.02, 34)
+        qa, sa = oracle.quant_tile_1x128(bf16_bits(dy), pow2=True)
+        _, qb, sb = oracle.quant_block_128x128(bf16_bits(w), pow2=True, transposed=True)
+        o, mop = oracle.DGRAD, mpq.DGRAD
+    else:
+        x = _bf16((K, M), 1.0, 35)                           # tokens x input features
+        dy = workloads.student_t3((K, N), 1e-3, g, "cpu")    # tokens x output features
+        qa, sa = oracle.quant_tile_128x1(bf16_bits(x), pow2=True)
+        qb, sb = oracle.quant_tile_128x1(bf16_bits(dy), pow2=True)
+        o, mop = oracle.WGRAD, mpq.WGRAD
+    args = (mop, _dev(qa), _dev(sa), _dev(qb), _dev(sb))
+    try:
+        mpq.mpq_set_gemm_stream_k(0)
+        dp = mpq.fp8_gemm_mx_pow2(*args, out_dtype=mpq.OUT_FP32)
+        mpq.mpq_set_gemm_stream_k(2)
+        sk1 = mpq.fp8_gemm_mx_pow2(*args, out_dtype=mpq.OUT_FP32)
+        sk2 = mpq.fp8_gemm_mx_pow2(*args, out_dtype=mpq.OUT_FP32)
+        torch.cuda.synchronize()
+        st, where = mpq.mpq_check_device_status()
+        assert st == 0, (st, where)
+    finally:
+        mpq.mpq_set_gemm_stream_k(1)
+    assert torch.equal(sk1, sk2)
+    d = dp.double()
+    assert float((sk1.double() - d).abs().max()) <= 1e-5 * float(d.abs().max())
+    rng = np.random.default_rng(36)
+    ms = np.unique(np.concatenate([rng.integers(0, M, 40), [0, 255, 256, M - 1]])).astype(np.int64)
+    ns = np.unique(np.concatenate([rng.integers(0, N, 40), [0, 255, 256, N - 1]])).astype(np.int64)
+    mm, nn = np.meshgrid(ms, ns, indexing="ij")
+    ref, absref = oracle.gemm_ref_at(o, qa, sa, qb, sb, mm.ravel(), nn.ravel())
+    got = sk1.cpu().numpy().astype(np.float64)[mm.ravel(), nn.ravel()]
+    assert_gemm_close(got, ref, absref, f"microscaling stream-K {op}")
+
+
 def test_mx_full_size_fprop_sampled(mpq):
     """The dense Fprop shape (4096 x 18432 x 7168) quantized on the GPU with power-of-2
     scales on both operands: codes and scales checked against the oracle on sampled rows,
