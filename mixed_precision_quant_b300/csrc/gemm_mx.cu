@@ -24,13 +24,17 @@
 //               columns 0-127, 128-255);
 //   warp 4      TMA producer: E4M3 slices into a 6-stage shared-memory ring;
 //   warp 5      MMA issuer (even CTA): once per four slices three tcgen05.cp of a slot into
-//               TMEM (in order with its MMAs); per slice four MMAs (K = 32 each) whose
-//               descriptor selects the slice's byte of the scale words, into one 256-column
-//               FP32 accumulator; one commit per slice (frees the operand stage), one per
-//               group of four (frees the scale slot) and one per tile (accumulator complete);
+//               TMEM (in order with its MMAs, one group ahead); per slice four MMAs (K = 32
+//               each) whose descriptor selects the slice's byte of the scale words, into one
+//               256-column FP32 accumulator; one commit per slice (frees the operand stage),
+//               one per group of four (frees the scale slot) and one per tile segment
+//               (accumulator complete);
 //   warps 8-15  epilogue: read the accumulator (32 lanes x 128 columns per warp) into
-//               registers, release it to the MMA issuer (the next tile's MMAs start), then
+//               registers, release it to the MMA issuer (the next segment's MMAs start), then
 //               write BF16 or FP32 through swizzled staging buffers and TMA stores.
+// Work order: whole tiles (data-parallel), or stream-K when the last wave of tiles would be
+// short -- the tile's later unit computes its last slices first and hands the FP32 partial
+// over; the earlier one adds it before the store (sched_device.cuh).
 // Every wait is bounded; a scale that is not a power of 2 in the UE8M0 range records
 // MPQ_ERR_SCALE in the status word.
 #include "mpq_internal.h"
