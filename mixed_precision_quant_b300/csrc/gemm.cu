@@ -26,13 +26,16 @@
 //   warp 0      TMA producer: E4M3 slices into a shared-memory ring (128-byte swizzle);
 //   warp 1      MMA issuer: four MMAs (K = 32 each) per 128-K slice into one of two TMEM
 //               partial buffers (2 x 256 columns), committed per slice;
-//   warp 2      scale loader: cp.async of the slice's A and B scales into an 8-slot ring;
+//   warp 2      scale loader: cp.async of the slice's A and B scales into a 4-slot ring;
 //   warps 4-11  promotion: tcgen05.ld the slice partial (two loads in flight), multiply
 //               by its two scales and accumulate into FP32 registers with scalar FMAs;
 //               promotion of slice k overlaps the MMAs of slice k+1.  The finished tile is
 //               written as BF16 or FP32 through swizzled staging buffers (two of 4 KB per
 //               warp in pair mode, so the stores drain while the next tile starts) and TMA
 //               bulk-tensor stores (32 rows x 128 bytes per store; 64 bytes single-SM).
+// Work order: whole tiles (data-parallel), or for dense GEMMs stream-K when the last wave of
+// tiles would be short (sched_device.cuh): a tile's later unit computes its last slices
+// first and hands the FP32 partial over, the earlier one adds it before the store.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its copies and MMAs, frees TMEM and exits.
 #include "mpq_internal.h"
