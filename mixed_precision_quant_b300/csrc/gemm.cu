@@ -51,6 +51,12 @@ constexpr int BK = 128;              // K per promotion slice
 constexpr int BN = 256;              // output columns per tile
 constexpr int SSLOTS = 4;            // scale ring depth (slices)
 constexpr int kThreads = 384;
+// The SwiGLU epilogue of pair tiles runs in four more warps (12-15), which take each tile's
+// BF16 gate / up values from shared memory while the promotion warps go on with the next
+// tile; single-SM and fused-quantization launches keep it in the promotion warps (their
+// shared memory has no room for the hand-over).
+__host__ __device__ constexpr bool sw_handoff(bool swiglu, bool pair, bool fuse) { return swiglu && pair && !fuse; }
+__host__ __device__ constexpr int threads_of(bool handoff) { return handoff ? 512 : kThreads; }
 constexpr uint32_t A_BYTES = 128 * BK;     // 128 rows of A per CTA per slice
 constexpr uint32_t TMEM_COLS = 512;        // two 256-column partial buffers
 constexpr int kMaxGroups = 1024;
@@ -83,7 +89,11 @@ struct Cfg {
     // SwiGLU epilogue: the two promotion warps of a lane quadrant exchange their rows'
     // half-group max-abs values (one barrier per quadrant, two arrivals)
     static constexpr int BAR_XCH = BAR_DRAIN + 1;
-    static constexpr int NBARS = BAR_XCH + 4;
+    // SwiGLU hand-over (pair tiles): a tile's gate / up values written (eight promotion warps)
+    // and consumed (four epilogue warps)
+    static constexpr int BAR_XFULL = BAR_XCH + 4;
+    static constexpr int BAR_XEMPTY = BAR_XFULL + 1;
+    static constexpr int NBARS = BAR_XEMPTY + 1;
     // Register split after the roles diverge (4 x 32 x low + 8 x 32 x high = 168 x 384, the
     // launch's allocation): for dense GEMMs with block B scales the producer, MMA and scale
     // warps run faster with 72 registers (Fprop +4%, Dgrad +1%); the per-column-scale
@@ -92,14 +102,17 @@ struct Cfg {
     {
         return scale_b != kScaleRowKN && !grouped;
     }
-    // The SwiGLU epilogue keeps more values live in the promotion warps: 40 / 232.
+    // The SwiGLU epilogue keeps more values live in the promotion warps: 40 / 232.  With the
+    // hand-over (512 threads, 128 registers each at launch): eight warps at 40 (producer, MMA,
+    // scale loader, idle, four epilogue) and the eight promotion warps at 216.
     __host__ __device__ static constexpr int regs_low(int scale_b, bool grouped, bool swiglu = false)
     {
         return swiglu ? 40 : wide_low(scale_b, grouped) ? 72 : 56;
     }
-    __host__ __device__ static constexpr int regs_high(int scale_b, bool grouped, bool swiglu = false)
+    __host__ __device__ static constexpr int regs_high(int scale_b, bool grouped, bool swiglu = false,
+                                                       bool handoff = false)
     {
-        return swiglu ? 232 : wide_low(scale_b, grouped) ? 216 : 224;
+        return handoff ? 216 : swiglu ? 232 : wide_low(scale_b, grouped) ? 216 : 224;
     }
     static constexpr size_t SMEM_MAIN = STAGES * STAGE_BYTES + 8 * OUT_BUFS * STAGE_OUT + SSLOTS * (128 + BN) * sizeof(float) +
                                         NBARS * sizeof(uint64_t) + 16;
@@ -130,6 +143,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     return true;
 }
 
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // acc[32 c + i] += partial column 32 c + i times its scales, for one 32-column chunk.
 // Scalar FMAs on purpose: the packed FP32x2 form runs on one of the SM's two FP32 pipes
 // only (four cycles per warp instruction), scalar FMAs use both -- half the pipe time for
@@ -149,11 +174,12 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
 }
 
 template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE, bool SK, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs p, const FuseArgs f)
 {
     using C = Cfg<PAIR>;
+    constexpr bool HANDOFF = sw_handoff(SWIGLU, PAIR, FUSE);
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -197,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::BAR_DRAIN), 1);
         for (int q = 0; q < 4; ++q)
             mbar_init(bar(C::BAR_XCH + q), 64);   // every thread of the quadrant's two warps
+        mbar_init(bar(C::BAR_XFULL), 8);          // this CTA's promotion warps
+        mbar_init(bar(C::BAR_XEMPTY), 4);         // the epilogue warps
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -322,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-    if (warp < 4) {
+    if (warp < 4 || warp >= 12) {   // warps 12-15: the SwiGLU hand-over's epilogue (pair tiles)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::regs_low(SCALE_B, GROUPED, SWIGLU)) : "memory");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
@@ -459,9 +487,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         scale_done:
             cp_async_wait_all();
+        } else if (HANDOFF && warp >= 12) {
+            // ---------------------------------------------------------- SwiGLU epilogue
+            // Thread er owns row er of this CTA's 128 tile rows and the tile's whole group of
+            // 128 output columns [n0, n0 + 128): x = silu(gate) * up of the BF16 values the
+            // promotion warps handed over, the group's max-abs and scale, 128 codes (and the
+            // BF16 gate / up row when it is kept).  Hand-over layout: row r at r * 512 bytes,
+            // the 16-byte chunk of columns 4j .. 4j+3 (a word per column, gate | up << 16) at
+            // chunk j ^ (r mod 32); the first pass overwrites each word with x in binary32.
+            const int er = (warp - 12) * 32 + lane;
+            const uint32_t rowb = smem_u32(smO) + static_cast<uint32_t>(er) * 512;
+            const uint32_t sw = static_cast<uint32_t>(er & 31);
+            uint32_t ec = 0;
+            Sched sc = sched_init(SK, unit, nunits, T, KB);
+            int t, kb0, kb1;
+            while (sched_next(sc, t, kb0, kb1)) {
+                const Tile ti = tile_of(t);
+                if (!mbar_wait_sleepy(bar(C::BAR_XFULL), ec & 1, ctl, 0x04E0))
+                    break;
+                const int m = ti.row0 + er;
+                if (m < ti.row_end) {
+                    __nv_bfloat16 *crow =
+                        p.C != nullptr ? static_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(m) * p.ldc : nullptr;
+                    float amax = 0.0f;
+#pragma unroll 4
+                    for (int j = 0; j < 32; ++j) {
+                        const uint32_t addr = rowb + ((static_cast<uint32_t>(j) ^ sw) << 4);
+                        const uint4 w = lds_v4(addr);
+                        float x0, x1, x2, x3;
+                        swiglu2(__uint_as_float(bf16x2_lo(w.x)), __uint_as_float(bf16x2_lo(w.y)),
+                                __uint_as_float(bf16x2_hi(w.x)), __uint_as_float(bf16x2_hi(w.y)), x0, x1);
+                        swiglu2(__uint_as_float(bf16x2_lo(w.z)), __uint_as_float(bf16x2_lo(w.w)),
+                                __uint_as_float(bf16x2_hi(w.z)), __uint_as_float(bf16x2_hi(w.w)), x2, x3);
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
+                        if (crow != nullptr) {   // the cached SwiGLU input: gate | up, BF16
+                            *reinterpret_cast<uint2 *>(crow + ti.n0 + 4 * j) =
+                                make_uint2((w.x & 0xFFFFu) | (w.y << 16), (w.z & 0xFFFFu) | (w.w << 16));
+                            *reinterpret_cast<uint2 *>(crow + p.sw_width + ti.n0 + 4 * j) =
+                                make_uint2((w.x >> 16) | (w.y & 0xFFFF0000u), (w.z >> 16) | (w.w & 0xFFFF0000u));
+                        }
+                        sts_v4(addr, __float_as_uint(x0), __float_as_uint(x1), __float_as_uint(x2), __float_as_uint(x3));
+                    }
+                    const GroupScale gs = make_group_scale(amax, p.sw_pow2 != 0);
+                    uint4 *qd = reinterpret_cast<uint4 *>(p.sw_q + static_cast<int64_t>(m) * p.sw_ldq + ti.n0);
+#pragma unroll 2
+                    for (int i = 0; i < 8; ++i) {   // sixteen codes per 16-byte store
+                        float xs[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = lds_v4(rowb + ((static_cast<uint32_t>(4 * i + c) ^ sw) << 4));
+                            xs[4 * c] = __uint_as_float(v.x);
+                            xs[4 * c + 1] = __uint_as_float(v.y);
+                            xs[4 * c + 2] = __uint_as_float(v.z);
+                            xs[4 * c + 3] = __uint_as_float(v.w);
+                        }
+                        uint32_t w4[4];
+                        codes_f32<16>(xs, gs, w4);
+                        qd[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    p.sw_s[static_cast<int64_t>(ti.n0 / 128) * p.sw_lds + m] = gs.s;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(C::BAR_XEMPTY));   // the hand-over area may be refilled
+                ++ec;
+            }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::regs_high(SCALE_B, GROUPED, SWIGLU)) : "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::regs_high(SCALE_B, GROUPED, SWIGLU, HANDOFF))
+                     : "memory");
         // -------------------------------------------------------------- promotion
         const int ew = warp - 4, quad = warp & 3, half = ew >> 2;
         const int row_in = quad * 32 + lane;
@@ -562,7 +656,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], v.w);
                 }
             }
-            if (SWIGLU) {
+            if constexpr (HANDOFF) {
+                // Hand the tile's gate and up values, rounded to BF16 (the values the plain
+                // grouped GEMM writes), to the epilogue warps: this thread's row, columns
+                // half * 64 .. +63 (chunks half * 16 .. +15 of the row's 32)
+                if (!mbar_wait(bar(C::BAR_XEMPTY), (xpar & 1) ^ 1, ctl, 0x04D0)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rowb = smem_u32(smO) + static_cast<uint32_t>(row_in) * 512;
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 gu = __floats2bfloat162_rn(acc[4 * c4 + k], acc[64 + 4 * c4 + k]);
+                        w[k] = *reinterpret_cast<const uint32_t *>(&gu);
+                    }
+                    const uint32_t j = static_cast<uint32_t>(half * 16 + c4);
+                    sts_v4(rowb + ((j ^ static_cast<uint32_t>(row_in & 31)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(C::BAR_XFULL));
+                ++xpar;
+                continue;
+            } else if (SWIGLU) {
                 // x = silu(gate) * up on the GEMM outputs rounded to BF16 (the values the plain
                 // grouped GEMM writes), then the 1x128 quantization of row m's group of output
                 // columns [n0, n0 + 128), whose other half the quadrant's other warp holds
@@ -757,7 +876,7 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
