@@ -51,12 +51,12 @@ constexpr int BK = 128;              // K per promotion slice
 constexpr int BN = 256;              // output columns per tile
 constexpr int SSLOTS = 4;            // scale ring depth (slices)
 constexpr int kThreads = 384;
-// The SwiGLU epilogue of pair tiles runs in four more warps (12-15), which take each tile's
-// BF16 gate / up values from shared memory while the promotion warps go on with the next
-// tile; single-SM and fused-quantization launches keep it in the promotion warps (their
-// shared memory has no room for the hand-over).
-__host__ __device__ constexpr bool sw_handoff(bool swiglu, bool pair, bool fuse) { return swiglu && pair && !fuse; }
-__host__ __device__ constexpr int threads_of(bool handoff) { return handoff ? 512 : kThreads; }
+// The SwiGLU epilogue runs in four more warps (12-15), which take each tile's BF16 gate / up
+// values from a 64 KB hand-over area in shared memory while the promotion warps go on with
+// the next tile.  Pair tiles use their output staging area for it; single-SM tiles make room
+// with a 3-stage operand ring.
+constexpr uint32_t kHandoffBytes = 128 * 128 * 4;   // 128 rows x 128 columns, gate | up words
+__host__ __device__ constexpr int threads_of(bool swiglu) { return swiglu ? 512 : kThreads; }
 constexpr uint32_t A_BYTES = 128 * BK;     // 128 rows of A per CTA per slice
 constexpr uint32_t TMEM_COLS = 512;        // two 256-column partial buffers
 constexpr int kMaxGroups = 1024;
@@ -86,12 +86,9 @@ struct Cfg {
     static constexpr int BAR_SFULL = BAR_TEMPTY + 2;
     static constexpr int BAR_SEMPTY = BAR_SFULL + SSLOTS;
     static constexpr int BAR_DRAIN = BAR_SEMPTY + SSLOTS;
-    // SwiGLU epilogue: the two promotion warps of a lane quadrant exchange their rows'
-    // half-group max-abs values (one barrier per quadrant, two arrivals)
-    static constexpr int BAR_XCH = BAR_DRAIN + 1;
-    // SwiGLU hand-over (pair tiles): a tile's gate / up values written (eight promotion warps)
-    // and consumed (four epilogue warps)
-    static constexpr int BAR_XFULL = BAR_XCH + 4;
+    // SwiGLU hand-over: a tile's gate / up values written (eight promotion warps) and
+    // consumed (four epilogue warps)
+    static constexpr int BAR_XFULL = BAR_DRAIN + 1;
     static constexpr int BAR_XEMPTY = BAR_XFULL + 1;
     static constexpr int NBARS = BAR_XEMPTY + 1;
     // Register split after the roles diverge (4 x 32 x low + 8 x 32 x high = 168 x 384, the
@@ -102,26 +99,38 @@ struct Cfg {
     {
         return scale_b != kScaleRowKN && !grouped;
     }
-    // The SwiGLU epilogue keeps more values live in the promotion warps: 40 / 232.  With the
-    // hand-over (512 threads, 128 registers each at launch): eight warps at 40 (producer, MMA,
-    // scale loader, idle, four epilogue) and the eight promotion warps at 216.
+    // SwiGLU (512 threads, 128 registers each at launch): eight warps at 40 (producer, MMA,
+    // scale loader, idle, the four epilogue warps) and the eight promotion warps at 216.
     __host__ __device__ static constexpr int regs_low(int scale_b, bool grouped, bool swiglu = false)
     {
         return swiglu ? 40 : wide_low(scale_b, grouped) ? 72 : 56;
     }
-    __host__ __device__ static constexpr int regs_high(int scale_b, bool grouped, bool swiglu = false,
-                                                       bool handoff = false)
+    __host__ __device__ static constexpr int regs_high(int scale_b, bool grouped)
     {
-        return handoff ? 216 : swiglu ? 232 : wide_low(scale_b, grouped) ? 216 : 224;
+        return wide_low(scale_b, grouped) ? 216 : 224;
     }
-    static constexpr size_t SMEM_MAIN = STAGES * STAGE_BYTES + 8 * OUT_BUFS * STAGE_OUT + SSLOTS * (128 + BN) * sizeof(float) +
-                                        NBARS * sizeof(uint64_t) + 16;
 };
 
 constexpr size_t kSmemGroups = (kMaxGroups + 1) * 2 * sizeof(int) + 16;
 
+// Operand stages and output-staging bytes of an instantiation: the SwiGLU hand-over needs a
+// 64 KB area, which pair tiles have as their staging area and single-SM tiles get by giving
+// up one of their four 48 KB stages.
 template <bool PAIR>
-size_t smem_bytes(bool grouped) { return 1024 + Cfg<PAIR>::SMEM_MAIN + (grouped ? kSmemGroups : 0); }
+__host__ __device__ constexpr int stages_of(bool swiglu) { return swiglu && !PAIR ? 3 : Cfg<PAIR>::STAGES; }
+template <bool PAIR>
+__host__ __device__ constexpr size_t staging_of(bool swiglu)
+{
+    return swiglu ? kHandoffBytes : static_cast<size_t>(8 * Cfg<PAIR>::OUT_BUFS * Cfg<PAIR>::STAGE_OUT);
+}
+template <bool PAIR>
+size_t smem_bytes(bool grouped, bool swiglu)
+{
+    using C = Cfg<PAIR>;
+    const size_t main = stages_of<PAIR>(swiglu) * C::STAGE_BYTES + staging_of<PAIR>(swiglu) +
+                        SSLOTS * (128 + BN) * sizeof(float) + C::NBARS * sizeof(uint64_t) + 16;
+    return 1024 + main + (grouped ? kSmemGroups : 0);
+}
 
 // Sizes are validated on the host to stay below 2^31 rows / columns.
 struct Tile {
@@ -174,20 +183,19 @@ __device__ __forceinline__ void promote_chunk(float (&acc)[128], const uint32_t 
 }
 
 template <int SCALE_B, bool OUT_F32, bool GROUPED, bool PAIR, bool FUSE, bool SK, bool SWIGLU>
-__global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
+__global__ void __launch_bounds__(threads_of(SWIGLU), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs p, const FuseArgs f)
 {
     using C = Cfg<PAIR>;
-    constexpr bool HANDOFF = sw_handoff(SWIGLU, PAIR, FUSE);
-    constexpr int STAGES = C::STAGES;
+    constexpr int STAGES = stages_of<PAIR>(SWIGLU);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *smA = base;
     uint8_t *smB = smA + STAGES * A_BYTES;
-    uint8_t *smO = smB + STAGES * C::B_BYTES;                    // output staging, 8 x OUT_BUFS x STAGE_OUT
-    float *ssa = reinterpret_cast<float *>(smO + 8 * C::OUT_BUFS * C::STAGE_OUT);
+    uint8_t *smO = smB + STAGES * C::B_BYTES;                    // output staging (SwiGLU: the hand-over area)
+    float *ssa = reinterpret_cast<float *>(smO + staging_of<PAIR>(SWIGLU));
     float *ssb = ssa + SSLOTS * 128;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ssb + SSLOTS * BN);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBARS);
@@ -221,8 +229,6 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
             mbar_init(bar(C::BAR_SEMPTY + j), 8);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
-        for (int q = 0; q < 4; ++q)
-            mbar_init(bar(C::BAR_XCH + q), 64);   // every thread of the quadrant's two warps
         mbar_init(bar(C::BAR_XFULL), 8);          // this CTA's promotion warps
         mbar_init(bar(C::BAR_XEMPTY), 4);         // the epilogue warps
         *abort_flag = 0;
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
-    if (warp < 4 || warp >= 12) {   // warps 12-15: the SwiGLU hand-over's epilogue (pair tiles)
+    if (warp < 4 || warp >= 12) {   // warps 12-15: the SwiGLU hand-over's epilogue
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::regs_low(SCALE_B, GROUPED, SWIGLU)) : "memory");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
             }
         scale_done:
             cp_async_wait_all();
-        } else if (HANDOFF && warp >= 12) {
+        } else if (SWIGLU && warp >= 12) {
             // ---------------------------------------------------------- SwiGLU epilogue
             // Thread er owns row er of this CTA's 128 tile rows and the tile's whole group of
             // 128 output columns [n0, n0 + 128): x = silu(gate) * up of the BF16 values the
@@ -554,7 +560,7 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
             }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::regs_high(SCALE_B, GROUPED, SWIGLU, HANDOFF))
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SWIGLU ? 216 : C::regs_high(SCALE_B, GROUPED))
                      : "memory");
         // -------------------------------------------------------------- promotion
         const int ew = warp - 4, quad = warp & 3, half = ew >> 2;
@@ -562,7 +568,7 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
         const uint32_t tm_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        uint32_t xpar = 0;   // SwiGLU epilogue: exchanges done
+        uint32_t xpar = 0;   // SwiGLU: tiles handed over
         Sched sc = sched_init(SK, unit, nunits, T, KB);
         int t, kb0, kb1;
         while (ok && sched_next(sc, t, kb0, kb1)) {
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
                     acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], v.w);
                 }
             }
-            if constexpr (HANDOFF) {
+            if constexpr (SWIGLU) {
                 // Hand the tile's gate and up values, rounded to BF16 (the values the plain
                 // grouped GEMM writes), to the epilogue warps: this thread's row, columns
                 // half * 64 .. +63 (chunks half * 16 .. +15 of the row's 32)
@@ -680,69 +686,6 @@ __global__ void __launch_bounds__(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1)
                 if (lane == 0)
                     mbar_arrive(bar(C::BAR_XFULL));
                 ++xpar;
-                continue;
-            } else if (SWIGLU) {
-                // x = silu(gate) * up on the GEMM outputs rounded to BF16 (the values the plain
-                // grouped GEMM writes), then the 1x128 quantization of row m's group of output
-                // columns [n0, n0 + 128), whose other half the quadrant's other warp holds
-                const int m = ti.row0 + quad * 32 + lane;
-                const bool valid = m < ti.row_end;
-                const int c0 = ti.n0 + half * 64;
-                // per 8 columns: round gate and up to BF16, store them when H is kept, and
-                // overwrite the gate accumulators with x (acc[0, 64) then holds x; keeps the
-                // register footprint at the accumulator's)
-                __nv_bfloat16 *crow = p.C != nullptr && valid
-                                          ? static_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(m) * p.ldc
-                                          : nullptr;
-                float amax = 0.0f;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t gw[4], uw[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int a = c8 * 8 + 2 * k;
-                        const __nv_bfloat162 g2 = __floats2bfloat162_rn(acc[a], acc[a + 1]);
-                        const __nv_bfloat162 u2 = __floats2bfloat162_rn(acc[64 + a], acc[64 + a + 1]);
-                        gw[k] = *reinterpret_cast<const uint32_t *>(&g2);
-                        uw[k] = *reinterpret_cast<const uint32_t *>(&u2);
-                    }
-                    if (crow != nullptr) {   // the cached SwiGLU input (gate | up), BF16
-                        *reinterpret_cast<uint4 *>(crow + c0 + c8 * 8) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
-                        *reinterpret_cast<uint4 *>(crow + p.sw_width + c0 + c8 * 8) =
-                            make_uint4(uw[0], uw[1], uw[2], uw[3]);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int a = c8 * 8 + 2 * k;
-                        swiglu2(__uint_as_float(bf16x2_lo(gw[k])), __uint_as_float(bf16x2_hi(gw[k])),
-                                __uint_as_float(bf16x2_lo(uw[k])), __uint_as_float(bf16x2_hi(uw[k])), acc[a],
-                                acc[a + 1]);
-                        amax = fmaxf(amax, fmaxf(fabsf(acc[a]), fabsf(acc[a + 1])));
-                    }
-                }
-                // the two half-group max-abs values of each row meet in shared memory (the
-                // output staging area, unused here; two buffers by exchange parity)
-                float *xch = reinterpret_cast<float *>(smO) + (xpar & 1) * 256;
-                xch[half * 128 + quad * 32 + lane] = amax;
-                mbar_arrive(bar(C::BAR_XCH + quad));
-                if (!mbar_wait(bar(C::BAR_XCH + quad), xpar & 1, ctl, 0x04C0 | quad)) {
-                    ok = false;
-                    break;
-                }
-                amax = fmaxf(amax, xch[(1 - half) * 128 + quad * 32 + lane]);
-                ++xpar;
-                const GroupScale gs = make_group_scale(amax, p.sw_pow2 != 0);
-                if (valid) {
-                    uint4 *qd = reinterpret_cast<uint4 *>(p.sw_q + static_cast<int64_t>(m) * p.sw_ldq + c0);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {   // sixteen codes per 16-byte store
-                        uint32_t w[4];
-                        codes_f32<16>(acc + 16 * i, gs, w);
-                        qd[i] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    if (half == 0)
-                        p.sw_s[static_cast<int64_t>(ti.n0 / 128) * p.sw_lds + m] = gs.s;
-                }
                 continue;
             }
             // Output: rows [ti.row0 + 32 quad, +32), columns [ti.n0 + 128 half, +128).  A warp
@@ -866,17 +809,17 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
                        const FuseArgs &f, int grid, cudaStream_t st)
 {
     auto kern = gemm_kernel<SB, F32, GR, PAIR, FUSE, SK, SWIGLU>;
-    const size_t smem = smem_bytes<PAIR>(GR);
+    const size_t smem = smem_bytes<PAIR>(GR, SWIGLU);
     static std::atomic<uint64_t> configured{0};   // per instantiation: devices already set up
     if (cudaError_t e = ensure_max_dyn_smem(kern, smem, configured); e != cudaSuccess)
         return e;
     if (!PAIR && !FUSE) {
-        kern<<<grid, kThreads, smem, st>>>(tmA, tmB, tmC, a, f);
+        kern<<<grid, threads_of(SWIGLU), smem, st>>>(tmA, tmB, tmC, a, f);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(threads_of(sw_handoff(SWIGLU, PAIR, FUSE)), 1, 1);
+    cfg.blockDim = dim3(threads_of(SWIGLU), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
