@@ -92,6 +92,31 @@ def test_swiglu_epilogue_equals_two_steps_and_oracle(mpq, tiles, counts, lead, t
     assert mpq.mpq_check_device_status() == (0, 0)
 
 
+def test_swiglu_epilogue_many_tiles_per_cta(mpq, tiles):
+    """About 16,000 rows over 8 experts, W = 512 (4 output tiles per m-tile): 500 single-SM
+    tiles on 148 SMs, 250 pair tiles on 74 pairs, so every CTA hands over three or four tiles
+    in turn through the same shared-memory area.  Bit-exact against GEMM + SwiGLU quantizer;
+    sampled rows bit-exact against the oracle's SwiGLU quantizer on the GPU's BF16 input."""
+    counts = [2100, 1900, 2050, 1999, 2001, 1950, 2048, 1950]
+    off, x_cpu, qb, sb = _problem(counts, 0, 0, 512, 256, 4242)
+    M = x_cpu.shape[0]
+    offs = _dev(off.astype(np.int64))
+    qx, sx = oracle.quant_tile_1x128(bf16_bits(x_cpu))
+    dqx, dsx, dqb, dsb = _dev(qx), _dev(sx), _dev(qb), _dev(sb)
+    q, s, H = mpq.fp8_grouped_gemm_swiglu_quant(offs, dqx, dsx, dqb, dsb, pow2=True, H=True)
+    C = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
+    mpq.fp8_grouped_gemm_blockscaled(offs, dqx, dsx, dqb, dsb, C=C, tiles="rows")
+    q2, s2 = mpq.fp8_swiglu_quant_1x128(C, pow2=True)
+    torch.cuda.synchronize()
+    assert mpq.mpq_check_device_status() == (0, 0)
+    assert torch.equal(H, C) and torch.equal(q, q2) and torch.equal(s, s2)
+    rows = np.unique(np.random.default_rng(7).integers(0, M, 64))
+    sel = torch.from_numpy(rows).cuda()
+    oq, os_ = oracle.swiglu_quant_1x128(bf16_bits(H[sel].cpu()), pow2=True)
+    assert np.array_equal(q[sel].cpu().numpy(), oq)
+    assert np.array_equal(s[:, sel].cpu().numpy(), os_)
+
+
 def test_swiglu_epilogue_without_cached_input(mpq):
     """H = None: only the codes and scales are written (the same values)."""
     off, x_cpu, qb, sb = _problem([70, 200], 0, 0, 256, 256, 31)
