@@ -457,6 +457,26 @@ def timed(fn, flush, reps=5, warm=2):
     return sum(ts) / len(ts)
 
 
+def timed_interleaved(fns, flush, reps=5, warm=2):
+    """Mean CUDA-event time of each function in ``fns``, their repetitions interleaved so that
+    each sees the same power and clock state (a milliseconds-long stretch of tensor work runs
+    under the board's power cap; timing one path after the other would favour the first)."""
+    import torch
+    for _ in range(warm):
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    ts = [[] for _ in fns]
+    for i in range(reps):
+        for k, fn in enumerate(fns):
+            flush(i)
+            a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+            a.record(); fn(); b.record()
+            torch.cuda.synchronize()
+            ts[k].append(a.elapsed_time(b))
+    return [sum(t) / len(t) for t in ts]
+
+
 def _acc_limited(ca, cb, bits, chunk=32):
     """sum_k ca[:, k] cb[:, k] in an accumulator with a `bits`-bit aligned window: for each
     chunk of 32 products (one tensor-core instruction's K on the pages' hardware), the running
@@ -655,20 +675,21 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
         res = {"tokens_routed": int(d["offsets"][-1]),
                "experts_nonempty": int((d["counts"] > 0).sum())}
         total_ms, total_flops, w_bytes, fused_ms = 0.0, 0.0, 0, 0.0
-        for proj, pow2 in (("up", False), ("down", True)):
-            X = d["X_up"] if proj == "up" else d["X_dn"]
-            Wt = d["W_up"] if proj == "up" else d["W_dn"]
+        weights = {}
+        for proj in ("up", "down"):   # 128x128 block quantization of both projections' weights
+            Wt = d.pop("W_up" if proj == "up" else "W_dn")
             G, N, K = Wt.shape
             qw = torch.empty((G, N, K), dtype=torch.uint8, device=dev)
             sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=dev)
             for e in range(G):
                 mpq.fp8_quant_block_128x128(Wt[e], q=qw[e], s=sw[e])
+            weights[proj] = (qw, sw)
             del Wt
-            if proj == "up":
-                del d["W_up"]
-            else:
-                del d["W_dn"]
             torch.cuda.empty_cache()
+        for proj, pow2 in (("up", False), ("down", True)):
+            X = d["X_up"] if proj == "up" else d["X_dn"]
+            qw, sw = weights[proj]
+            G, N, K = qw.shape
             qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X, pow2=pow2)
             C = torch.empty((X.shape[0], N), dtype=torch.bfloat16, device=dev)
 
@@ -717,8 +738,49 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
             total_ms += ms
             total_flops += fl
             w_bytes += wb
-            del qw, sw, qx, sx, C
+            del qx, sx, C
             torch.cuda.empty_cache()
+        # The whole MoE FFN: up projection, SwiGLU + pow2 1x128 quantization, down projection on
+        # those codes -- as separate kernels, and with SwiGLU + quantization in the up GEMM's
+        # epilogue (prefill: after the 1x128 quantizer; decode: one launch from the BF16 rows)
+        (qwu, swu), (qwd, swd) = weights["up"], weights["down"]
+        X = d["X_up"]
+        rows, W = X.shape[0], qwu.shape[1] // 2
+        qx, sx, _, _ = mpq.fp8_quant_tile_1x128(X)
+        H = torch.empty((rows, 2 * W), dtype=torch.bfloat16, device=dev)
+        sq = torch.empty((rows, W), dtype=torch.uint8, device=dev)
+        ss = torch.empty((W // 128, rows), dtype=torch.float32, device=dev)
+        Y = torch.empty((rows, qwd.shape[1]), dtype=torch.bfloat16, device=dev)
+        decode = name == "moe_decode"
+
+        def layer_two_step():
+            if decode:
+                mpq.fp8_grouped_gemm_blockscaled(off, X, None, qwu, swu, C=H, fuse_quant=True)
+            else:
+                mpq.fp8_quant_tile_1x128(X, q=qx, s=sx)
+                mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qwu, swu, C=H)
+            mpq.fp8_swiglu_quant_1x128(H, pow2=True, q=sq, s=ss)
+            mpq.fp8_grouped_gemm_blockscaled(off, sq, ss, qwd, swd, C=Y)
+
+        def layer_fused():
+            if decode:
+                mpq.fp8_grouped_gemm_swiglu_quant(off, X, None, qwu, swu, pow2=True, q=sq, s=ss, fuse_quant=True)
+            else:
+                mpq.fp8_quant_tile_1x128(X, q=qx, s=sx)
+                mpq.fp8_grouped_gemm_swiglu_quant(off, qx, sx, qwu, swu, pow2=True, q=sq, s=ss)
+            mpq.fp8_grouped_gemm_blockscaled(off, sq, ss, qwd, swd, C=Y)
+
+        lt, lf = timed_interleaved((layer_two_step, layer_fused), flush)
+        res["layer"] = {"two_step_ms": round(lt, 4), "fused_ms": round(lf, 4),
+                        "TFLOPs_two_step": round(total_flops / lt / 1e9, 1),
+                        "TFLOPs_fused": round(total_flops / lf / 1e9, 1),
+                        "frac_fp8_peak_fused": round(total_flops / lf / 1e9 / fp8_peak, 4),
+                        "frac_hbm_weights_fused": round(gb(w_bytes, lf) / hbm, 4),
+                        "path": "BF16 rows in, " + ("fused quantization + " if decode else "1x128 quantizer + ") +
+                                "up GEMM, SwiGLU + pow2 1x128 quantization (own kernel / in the up GEMM's "
+                                "epilogue), down GEMM on those codes, BF16 out"}
+        del qx, sx, H, sq, ss, Y, weights, qwu, swu, qwd, swd
+        torch.cuda.empty_cache()
         res["total_ms"] = round(total_ms, 4)
         res["TFLOPs"] = round(total_flops / total_ms / 1e9, 1)
         res["frac_fp8_peak"] = round(total_flops / total_ms / 1e9 / fp8_peak, 4)
