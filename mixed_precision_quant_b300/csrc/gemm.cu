@@ -308,8 +308,10 @@ __global__ void __launch_bounds__(threads_of(SWIGLU), 1)
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
 
-    if (FUSE)   // fused activation quantization: phase 1, all warps, before the roles split
-        quantize_rows_phase(goff, p.G, M, KB, p.K, f);
+    // fused activation quantization: phase 1, all warps, before the roles split (SwiGLU: 512
+    // threads at 128 registers each, one group a lane per batch)
+    if (FUSE)
+        quantize_rows_phase<SWIGLU ? 1 : 2>(goff, p.G, M, KB, p.K, f);
 
     const int MT = static_cast<int>((M + C::TILE_M - 1) / C::TILE_M);
     const int T = GROUPED ? gtile[p.G] : MT * NT;

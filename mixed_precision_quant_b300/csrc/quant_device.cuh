@@ -148,10 +148,11 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 // shuffles across the LPG lanes.  Lanes handle U groups per batch and load the next batch
 // before converting the current one.  When its range is done the CTA publishes it by a
 // fence and an atomic add to the ready count of every expert the range overlaps.
+template <int U = 2>
 __device__ __forceinline__ void quantize_rows_phase(const int *goff, int G, int64_t M, int KB, int64_t K,
                                                     const FuseArgs &f)
 {
-    constexpr int LPG = 4, CPL = 16 / LPG, U = 8 / CPL;
+    constexpr int LPG = 4, CPL = 16 / LPG;
     const int r_begin = goff[0], r_end = goff[G];
     const int per_cta = (r_end - r_begin + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int r0 = min(r_end, r_begin + static_cast<int>(blockIdx.x) * per_cta);
