@@ -71,7 +71,7 @@ class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,temperature.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -104,7 +104,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, watts, temp = [], [], set(), [], []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -114,13 +114,23 @@ class ClockSampler:
                 sm.append(float(parts[1])); mx.append(float(parts[2]))
             except ValueError:
                 continue
+            for dst, i in ((watts, 3), (temp, 9)):
+                try:
+                    dst.append(float(parts[i]))
+                except (ValueError, IndexError):
+                    pass
             for nm, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if watts:
+            out["power_w_median"] = statistics.median(watts)
+        if temp:
+            out["temp_c"] = [min(temp), max(temp)]
+        return out
 
 
 # ------------------------------------------------------------------ helpers
@@ -442,30 +452,37 @@ def measure_fp8_cublas(dev, shapes=((8192, 8192, 8192), (M_DENSE, N_DENSE, K_DEN
     return out
 
 
-def timed(fn, flush, reps=5, warm=2):
+ROW_REPS = 10          # flushed repetitions per row; the row reports their median
+ROW_WARM_MS = 25.0     # device time a row spends warming up before its first timed repetition
+
+
+def _warm(fns):
+    """Runs ``fns`` at least twice and until about ROW_WARM_MS of device time has passed, so
+    the first timed repetition does not meet a clock still ramping up after a pause."""
     import torch
-    for _ in range(warm):
-        fn()
-    torch.cuda.synchronize()
-    ts = []
-    for i in range(reps):
-        flush(i)
-        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
-        a.record(); fn(); b.record()
+    a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+    spent, n = 0.0, 0
+    while n < 2 or (spent < ROW_WARM_MS and n < 200):
+        a.record()
+        for fn in fns:
+            fn()
+        b.record()
         torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return sum(ts) / len(ts)
+        spent += a.elapsed_time(b)
+        n += 1
 
 
-def timed_interleaved(fns, flush, reps=5, warm=2):
-    """Mean CUDA-event time of each function in ``fns``, their repetitions interleaved so that
+def timed(fn, flush, reps=ROW_REPS):
+    """Median CUDA-event time (ms) of ``fn`` over ``reps`` repetitions, L2 flushed before each."""
+    return timed_interleaved((fn,), flush, reps)[0]
+
+
+def timed_interleaved(fns, flush, reps=ROW_REPS):
+    """Median CUDA-event time of each function in ``fns``, their repetitions interleaved so that
     each sees the same power and clock state (a milliseconds-long stretch of tensor work runs
     under the board's power cap; timing one path after the other would favour the first)."""
     import torch
-    for _ in range(warm):
-        for fn in fns:
-            fn()
-    torch.cuda.synchronize()
+    _warm(fns)
     ts = [[] for _ in fns]
     for i in range(reps):
         for k, fn in enumerate(fns):
@@ -474,7 +491,7 @@ def timed_interleaved(fns, flush, reps=5, warm=2):
             a.record(); fn(); b.record()
             torch.cuda.synchronize()
             ts[k].append(a.elapsed_time(b))
-    return [sum(t) / len(t) for t in ts]
+    return [statistics.median(t) for t in ts]
 
 
 def _acc_limited(ca, cb, bits, chunk=32):
@@ -563,6 +580,7 @@ def accuracy_vs_k(mpq, workloads, dev, ks=(512, 1024, 2048, 4096, 8192, 16384), 
 def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe", "mx", "accuracy")):
     """Time every other hot-path step on its configuration (CUDA events, L2 flushed).
     ``groups`` selects the backward-pair rows, the MoE rows and the accuracy report."""
+    import torch
     hbm = peaks["hbm_gbs"]
     flush = L2Flush(dev)
     out = {}
@@ -570,12 +588,22 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe"
     def gb(nbytes, ms):
         return nbytes / (ms / 1e3) / 1e9
 
-    if "backward" in groups:
-        _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)
-    if "moe" in groups:
-        _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)
-    if "mx" in groups:
-        _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)
+    # Each group of rows starts after a 2 s idle pause (a long stretch of GEMMs before it can
+    # leave the board power- or heat-limited) and is timed with its own clock record.
+    runs = (("backward", lambda: _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
+            ("moe", lambda: _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
+            ("mx", lambda: _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)))
+    clocks = {}
+    for g, run in runs:
+        if g not in groups:
+            continue
+        torch.cuda.synchronize(dev)
+        time.sleep(2.0)
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+            run()
+        clocks[g] = clk.summary()
+    if clocks:
+        out["clocks_by_group"] = clocks
     if "accuracy" in groups:
         out["accuracy_vs_K"] = accuracy_vs_k(mpq, workloads, dev)
     return out
