@@ -618,8 +618,9 @@ def _mx_rows(mpq, workloads, dev, flush, fp8_peak, out):
     def row(name, op, qa, sa, qb, sb, od, flops):
         C = torch.empty((qa.shape[0], qb.shape[0]), dtype=torch.float32 if od == mpq.OUT_FP32 else torch.bfloat16,
                         device=dev)
-        ms_mx = timed(lambda: mpq.fp8_gemm_mx_pow2(op, qa, sa, qb, sb, out_dtype=od, C=C), flush)
-        ms_sw = timed(lambda: mpq.fp8_gemm_blockscaled(op, qa, sa, qb, sb, out_dtype=od, C=C), flush)
+        ms_mx, ms_sw = timed_interleaved((lambda: mpq.fp8_gemm_mx_pow2(op, qa, sa, qb, sb, out_dtype=od, C=C),
+                                          lambda: mpq.fp8_gemm_blockscaled(op, qa, sa, qb, sb, out_dtype=od, C=C)),
+                                         flush)
         st, where = mpq.mpq_check_device_status()
         if st != 0:
             raise RuntimeError(f"device status {st} at {where:#x} in {name}")
@@ -725,43 +726,53 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out):
                 mpq.fp8_quant_tile_1x128(X, pow2=pow2, q=qx, s=sx)
                 mpq.fp8_grouped_gemm_blockscaled(off, qx, sx, qw, sw, C=C)
 
-            ms = timed(run, flush)
+            # Every path of this projection is timed in one interleaved loop, so that all of them
+            # see the same power state (HBM-bound decode brings the board to its power cap
+            # within tens of milliseconds; whatever is timed later would run at lower clocks).
+            fns = {"two_step": run}
+            if name == "moe_decode":
+                # the same projection as one fused launch: BF16 rows in, quantized on the fly
+                fns["fused"] = lambda: mpq.fp8_grouped_gemm_blockscaled(off, X, None, qw, sw, C=C, fuse_quant=True,
+                                                                        pow2=pow2)
+            if proj == "up":
+                # SwiGLU of this up-projection output (gate | up halves) fused with the pow2
+                # 1x128 quantization that feeds the down projection: as its own kernel after the
+                # GEMM, and in the GEMM's epilogue (one launch; the BF16 SwiGLU input is not written)
+                sq, ss = mpq.fp8_swiglu_quant_1x128(C, pow2=True)
+                gemm = fns.get("fused", run)
+                fns["swiglu"] = lambda: mpq.fp8_swiglu_quant_1x128(C, pow2=True, q=sq, s=ss)
+                fns["up_two_step"] = lambda: (gemm(), mpq.fp8_swiglu_quant_1x128(C, pow2=True, q=sq, s=ss))
+                fused_args = (off, X, None, qw, sw) if name == "moe_decode" else (off, qx, sx, qw, sw)
+                fns["epilogue"] = lambda: mpq.fp8_grouped_gemm_swiglu_quant(*fused_args, pow2=True, q=sq, s=ss,
+                                                                            fuse_quant=name == "moe_decode")
+            tm = dict(zip(fns, timed_interleaved(list(fns.values()), flush)))
+            ms = tm["two_step"]
             fl = 2.0 * X.shape[0] * N * K
             wb = G * N * K + G * (N // 128) * (K // 128) * 4
             res[proj] = {"ms": round(ms, 4), "TFLOPs": round(fl / ms / 1e9, 1),
                          "frac_fp8_peak": round(fl / ms / 1e9 / fp8_peak, 4),
                          "weight_GBps": round(gb(wb, ms), 1), "frac_hbm_weights": round(gb(wb, ms) / hbm, 4),
                          "path": "1x128 quantizer + grouped GEMM (tiling chosen by the library)"}
-            if name == "moe_decode":
-                # the same projection as one fused launch: BF16 rows in, quantized on the fly
-                fms = timed(lambda: mpq.fp8_grouped_gemm_blockscaled(off, X, None, qw, sw, C=C, fuse_quant=True,
-                                                                     pow2=pow2), flush)
+            if "fused" in tm:
+                fms = tm["fused"]
                 res[proj]["fused"] = {"ms": round(fms, 4), "weight_GBps": round(gb(wb, fms), 1),
                                       "frac_hbm_weights": round(gb(wb, fms) / hbm, 4),
                                       "path": "one cooperative launch: 1x128 quantization phase + row-tile grouped GEMM"}
                 fused_ms += fms
             if proj == "up":
-                # SwiGLU of this up-projection output (gate | up halves) fused with the pow2
-                # 1x128 quantization that feeds the down projection
-                sq, ss = mpq.fp8_swiglu_quant_1x128(C, pow2=True)
-                sms = timed(lambda: mpq.fp8_swiglu_quant_1x128(C, pow2=True, q=sq, s=ss), flush)
+                sms, efms = tm["swiglu"], tm["epilogue"]
                 nbytes = X.shape[0] * (N // 2) * (4 + 1 + 4 / 128)
                 res["swiglu_quant"] = {"ms": round(sms, 4), "GBps": round(gb(nbytes, sms), 1),
                                        "frac_hbm": round(gb(nbytes, sms) / hbm, 4), "bound": "hbm",
                                        "shape": [int(X.shape[0]), int(N)]}
-                # the same up projection with SwiGLU + pow2 quantization in the GEMM epilogue
-                # (one launch; the BF16 SwiGLU input is not written), against the two steps
-                # above (GEMM with BF16 output, then SwiGLU + quantization)
-                fused_args = (off, X, None, qw, sw) if name == "moe_decode" else (off, qx, sx, qw, sw)
-                efms = timed(lambda: mpq.fp8_grouped_gemm_swiglu_quant(*fused_args, pow2=True, q=sq, s=ss,
-                                                                       fuse_quant=name == "moe_decode"), flush)
-                two = (res[proj]["fused"]["ms"] if name == "moe_decode" else ms) + sms
                 res["up_swiglu_epilogue"] = {
-                    "ms": round(efms, 4), "two_step_ms": round(two, 4),
+                    "ms": round(efms, 4), "two_step_ms": round(tm["up_two_step"], 4),
                     "TFLOPs": round(fl / efms / 1e9, 1), "frac_fp8_peak": round(fl / efms / 1e9 / fp8_peak, 4),
                     "path": ("one cooperative launch: 1x128 quantization of the BF16 rows + grouped GEMM + SwiGLU "
                              "+ pow2 1x128 quantization" if name == "moe_decode" else
-                             "grouped GEMM with SwiGLU + pow2 1x128 quantization in the epilogue (codes + scales out)")}
+                             "grouped GEMM with SwiGLU + pow2 1x128 quantization in the epilogue (codes + scales out)"),
+                    "two_step_path": ("fused quantization + GEMM launch" if name == "moe_decode" else
+                                      "1x128 quantizer + grouped GEMM") + ", then the SwiGLU quantizer kernel"}
                 del sq, ss
             total_ms += ms
             total_flops += fl
