@@ -149,16 +149,23 @@ __device__ __forceinline__ void produce128(uint32_t stage, uint32_t bars, int st
 
 // ------------------------------------------------------------------ 1x128 rows
 //
-// One 128-row x 128-column tile per ring slot (four slots); warpgroup h (threads
-// 128h .. +127) takes the CTA's tiles h, h+2, ..., thread rr owning row rr of the tile, with
-// its own barrier and two staging boxes used in turn, so the two warpgroups run
-// independently and a tile's store drains while the next tile is converted.
+// One 128-row x 128-column tile per ring slot (four slots); warpgroup h (warps 8h .. 8h+7,
+// threads 256h .. +255) takes the CTA's tiles h, h+2, ..., with its own barrier and two
+// staging boxes used in turn, so the two warpgroups run independently and a tile's store
+// drains while the next tile is converted.  Thread u of a warpgroup owns half a row group:
+// row u/2, columns 64 (u%2) .. +63 (one of the tile's two 128 x 64 boxes), and the two
+// halves' max-abs values meet in one shuffle -- sixteen consumer warps where one thread per
+// row (64 words of data) left room for eight (131072 x 7168: 6.08 against 5.95 TB/s; small
+// tensors such as 4096 x 7168, twelve tiles per SM, are set by the first load and the last
+// store rather than by the conversion).
 constexpr int QR_STAGES = 4;
 static_assert(QR_STAGES % 2 == 0, "a stage must belong to one of the two warpgroups");
+constexpr int kRowsConsumers = 16;
+constexpr int kRowsThreads = 32 * (kRowsConsumers + 1);
 constexpr size_t kRowsSmem = 1024 + QR_STAGES * 2 * kBox + 4 * kBox + (2 * QR_STAGES + 2) * 8 + 16;
 
 template <bool POW2>
-__global__ void __launch_bounds__(kQThreads, 1)
+__global__ void __launch_bounds__(kRowsThreads, 1)
     quant_rows_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
                       const QuantArgs p)
 {
@@ -172,10 +179,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < QR_STAGES; ++i) {
             mbar_init(bars + 8 * i, 1);
-            mbar_init(bars + 8 * (QR_STAGES + i), 4);  // the four warps of one warpgroup
+            mbar_init(bars + 8 * (QR_STAGES + i), 8);  // the eight warps of one warpgroup
         }
-        mbar_init(bars + 8 * (2 * QR_STAGES), 4);
-        mbar_init(bars + 8 * (2 * QR_STAGES + 1), 4);
+        mbar_init(bars + 8 * (2 * QR_STAGES), 8);
+        mbar_init(bars + 8 * (2 * QR_STAGES + 1), 8);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -183,14 +190,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
     const int64_t ncb = p.cols / 128, items = ((p.rows + 127) / 128) * ncb;
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    if (warp == kConsumers) {
+    if (warp == kRowsConsumers) {
         if (lane == 0)
             produce128(stage, bars, QR_STAGES, &tmx, items, ncb, ctl, p.timeout_ns, 0x1100);
         return;
     }
-    const int h = t >> 7, rr = t & 127;
+    const int h = t >> 8, u = t & 255;
+    const int rr = u >> 1, sub = u & 1;                 // row and column half
     const uint32_t wgbar = bars + 8 * (2 * QR_STAGES + h);
-    const bool elected = rr == 0;
+    const bool elected = u == 0;
     uint32_t cph = 0;
     uint32_t it = h;   // this warpgroup's tiles are the CTA's tiles h, h + 2, ...
     for (int64_t item = blockIdx.x + h * static_cast<int64_t>(gridDim.x); item < items;
@@ -200,20 +208,29 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
         const int64_t rb = item / ncb, kb = item - rb * ncb;
         const uint32_t out = out_rows + (2 * h + ((it >> 1) & 1)) * kBox;   // this tile's staging box
-        uint32_t w[64];
-        load_row(stage + st * 2 * kBox, rr, w);
+        uint32_t w[32];
+        const uint32_t box = stage + st * 2 * kBox + sub * kBox;   // columns 64 sub .. +63
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = lds_v4(box + sw128(rr, j));
+            w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+        }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(bars + 8 * (QR_STAGES + st));
-        const GroupScale g = make_group_scale(amax_words(w), POW2);
+        float a = amax_words(w);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const GroupScale g = make_group_scale(a, POW2);
         const int64_t r = rb * 128 + rr;
-        if (r < p.rows)
+        if (sub == 0 && r < p.rows)
             p.s[kb * p.lds + r] = g.s;
         if (elected)
             bulk_wait_read1();                 // the box's previous store has left it
         if (!wg_sync(wgbar, cph, ctl, 0x1210))
             break;
-        write_codes(out, rr, w, g);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            sts_v4(out + sw128(rr, sub * 4 + q), codes16(&w[q * 8], g));
         fence_proxy_async_smem();
         if (!wg_sync(wgbar, cph, ctl, 0x1211))
             break;
@@ -706,8 +723,8 @@ cudaError_t launch_quant_rows(const CUtensorMap &tmx, const CUtensorMap &tmq, co
     if (items == 0)
         return cudaSuccess;
     constexpr size_t smem = kRowsSmem;
-    return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, kQThreads, tmx, tmq, a)
-                : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, kQThreads, tmx, tmq, a);
+    return pow2 ? launch_q(quant_rows_kernel<true>, smem, items, num_sms, st, kRowsThreads, tmx, tmq, a)
+                : launch_q(quant_rows_kernel<false>, smem, items, num_sms, st, kRowsThreads, tmx, tmq, a);
 }
 
 cudaError_t launch_quant_dual(const CUtensorMap &tmx, const CUtensorMap &tmq, const CUtensorMap &tmqT,
