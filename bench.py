@@ -378,7 +378,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     fp8_cublas = measure_fp8_cublas(dev)
     cub = fp8_cublas.get("8192x8192x8192")
-    groups = set(args.rows.split(",")) if args.rows else {"backward", "moe", "mx", "accuracy"}
+    groups = set(args.rows.split(",")) if args.rows else {"sustained", "backward", "moe", "mx", "accuracy"}
     rows = {} if args.no_rows else measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups)
 
     result = {
@@ -577,9 +577,10 @@ def accuracy_vs_k(mpq, workloads, dev, ks=(512, 1024, 2048, 4096, 8192, 16384), 
     return out
 
 
-def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe", "mx", "accuracy")):
+def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("sustained", "backward", "moe", "mx", "accuracy")):
     """Time every other hot-path step on its configuration (CUDA events, L2 flushed).
-    ``groups`` selects the backward-pair rows, the MoE rows and the accuracy report."""
+    ``groups`` selects the sustained dense step, the backward-pair rows, the MoE rows, the
+    microscaling rows and the accuracy report."""
     import torch
     hbm = peaks["hbm_gbs"]
     flush = L2Flush(dev)
@@ -590,7 +591,9 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe"
 
     # Each group of rows starts after a 2 s idle pause (a long stretch of GEMMs before it can
     # leave the board power- or heat-limited) and is timed with its own clock record.
-    runs = (("backward", lambda: _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
+    runs = (("sustained", lambda: _sustained_rows(mpq, workloads, dev, fp8_peak,
+                                                  peaks["bf16_tflops_sustained"] * FP8_PER_BF16, out)),
+            ("backward", lambda: _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
             ("moe", lambda: _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak,
                                       peaks["bf16_tflops_sustained"] * FP8_PER_BF16, gb, out)),
             ("mx", lambda: _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)))
@@ -608,6 +611,53 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("backward", "moe"
     if "accuracy" in groups:
         out["accuracy_vs_K"] = accuracy_vs_k(mpq, workloads, dev)
     return out
+
+
+def _sustained_rows(mpq, workloads, dev, fp8_peak, fp8_sustained, out, steps=2400):
+    """The dense Fprop step run back to back for about a second and a quarter, long enough
+    for the board's power limit to act: the mean of the second half of the steps, against
+    the sustained FP8 rate (2 x the measured sustained BF16 rate) beside the burst one.  The
+    step's inputs (323 MB of BF16) exceed L2, so no flush runs between steps here."""
+    import torch
+    d = workloads.dense_fprop(device=dev)
+    A, W = d["A"], d["W"]
+    M, K = A.shape
+    N = W.shape[0]
+    qa, sa, _, _ = mpq.fp8_quant_tile_1x128(A)
+    qb, _, sb = mpq.fp8_quant_block_128x128(W)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = [(ev(), ev(), ev()) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        e0, e1, e2 = marks[i]
+        e0.record()
+        mpq.fp8_quant_tile_1x128(A, q=qa, s=sa)
+        mpq.fp8_quant_block_128x128(W, q=qb, s=sb)
+        e1.record()
+        mpq.fp8_gemm_blockscaled(mpq.FPROP, qa, sa, qb, sb, C=C)
+        e2.record()
+    torch.cuda.synchronize(dev)
+    st, where = mpq.mpq_check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at {where:#x} in the sustained run")
+    half = marks[steps // 2:]
+    step_ms = sum(m[0].elapsed_time(m[2]) for m in half) / len(half)
+    gemm_ms = sum(m[1].elapsed_time(m[2]) for m in half) / len(half)
+    first = marks[:50]
+    first_gemm_ms = sum(m[1].elapsed_time(m[2]) for m in first) / len(first)
+    fl = 2.0 * M * N * K
+    out["dense_fprop_sustained"] = {
+        "steps": steps, "timed_steps": len(half), "ms_per_step": round(step_ms, 4),
+        "TFLOPs_step": round(fl / step_ms / 1e9, 1), "gemm_ms": round(gemm_ms, 4),
+        "gemm_TFLOPs": round(fl / gemm_ms / 1e9, 1),
+        "gemm_frac_fp8_sustained": round(fl / gemm_ms / 1e9 / fp8_sustained, 4),
+        "gemm_frac_fp8_peak": round(fl / gemm_ms / 1e9 / fp8_peak, 4),
+        "first_50_gemm_TFLOPs": round(fl / first_gemm_ms / 1e9, 1),
+        "fp8_sustained_tflops": round(fp8_sustained, 1),
+        "note": "no L2 flush (inputs exceed L2); mean of the second half of the steps"}
+    del d, A, W, qa, sa, qb, sb, C
+    torch.cuda.empty_cache()
 
 
 def _mx_rows(mpq, workloads, dev, flush, fp8_peak, out):
@@ -1017,7 +1067,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--rows", default="", help="comma list of row groups to measure: backward, moe, mx, accuracy "
+    ap.add_argument("--rows", default="", help="comma list of row groups to measure: sustained, backward, moe, mx, accuracy "
                     "(default: all)")
     ap.add_argument("--profile", choices=PROFILE_CASES, default=None,
                     help="launch one kernel on a small case for an ncu capture (no timing, no JSON line)")
