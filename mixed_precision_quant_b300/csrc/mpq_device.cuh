@@ -514,6 +514,20 @@ __device__ __forceinline__ uint32_t e4m3x2(float first, float second)
     return r;
 }
 
+// Four binary32 values -> four E4M3 codes in one word, byte k holding value k (the two
+// 16-bit halves joined by one vector move instead of a shift and an or).
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_lo(uint32_t w) { return w << 16; }
 __device__ __forceinline__ uint32_t bf16x2_hi(uint32_t w) { return w & 0xFFFF0000u; }
 

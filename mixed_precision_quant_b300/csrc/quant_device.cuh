@@ -35,33 +35,33 @@ __device__ __forceinline__ float amax_words(const uint32_t (&w)[N])
 template <int NW>
 __device__ __forceinline__ void codes_words(const uint32_t *w, const GroupScale &g, uint32_t *out)
 {
-    uint32_t c[NW];
-    uint32_t flip = 0;
     if (g.mode == 0) {
         const unsigned long long nr = pack2(-g.r, -g.r), s2 = pack2(g.s, g.s);
 #pragma unroll
-        for (int j = 0; j < NW; ++j) {
-            const unsigned long long t =
-                neg_quotient2(pack2(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j]))), nr, s2);
-            c[j] = e4m3x2(lo_of(t), hi_of(t));
+        for (int j = 0; j < NW / 2; ++j) {
+            const unsigned long long t0 = neg_quotient2(
+                pack2(__uint_as_float(bf16x2_lo(w[2 * j])), __uint_as_float(bf16x2_hi(w[2 * j]))), nr, s2);
+            const unsigned long long t1 = neg_quotient2(
+                pack2(__uint_as_float(bf16x2_lo(w[2 * j + 1])), __uint_as_float(bf16x2_hi(w[2 * j + 1]))), nr, s2);
+            out[j] = e4m3x4(lo_of(t0), hi_of(t0), lo_of(t1), hi_of(t1)) ^ 0x80808080u;
         }
-        flip = 0x80808080u;
     } else if (g.mode == 1) {
         const unsigned long long r = pack2(g.r, g.r);
 #pragma unroll
-        for (int j = 0; j < NW; ++j) {
-            const unsigned long long p =
-                fmul2(pack2(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j]))), r);
-            c[j] = e4m3x2(lo_of(p), hi_of(p));
+        for (int j = 0; j < NW / 2; ++j) {
+            const unsigned long long p0 =
+                fmul2(pack2(__uint_as_float(bf16x2_lo(w[2 * j])), __uint_as_float(bf16x2_hi(w[2 * j]))), r);
+            const unsigned long long p1 =
+                fmul2(pack2(__uint_as_float(bf16x2_lo(w[2 * j + 1])), __uint_as_float(bf16x2_hi(w[2 * j + 1]))), r);
+            out[j] = e4m3x4(lo_of(p0), hi_of(p0), lo_of(p1), hi_of(p1));
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < NW; ++j)
-            c[j] = e4m3_pair(__uint_as_float(bf16x2_lo(w[j])), __uint_as_float(bf16x2_hi(w[j])), g);
+        for (int j = 0; j < NW / 2; ++j)
+            out[j] = e4m3_pair(__uint_as_float(bf16x2_lo(w[2 * j])), __uint_as_float(bf16x2_hi(w[2 * j])), g) |
+                     (e4m3_pair(__uint_as_float(bf16x2_lo(w[2 * j + 1])), __uint_as_float(bf16x2_hi(w[2 * j + 1])), g)
+                      << 16);
     }
-#pragma unroll
-    for (int j = 0; j < NW / 2; ++j)
-        out[j] = (c[2 * j] | (c[2 * j + 1] << 16)) ^ flip;
 }
 
 // N binary32 values (consecutive in the output row) -> N E4M3 codes (N/4 words), the
@@ -69,31 +69,27 @@ __device__ __forceinline__ void codes_words(const uint32_t *w, const GroupScale 
 template <int N>
 __device__ __forceinline__ void codes_f32(const float *x, const GroupScale &g, uint32_t *out)
 {
-    uint32_t c[N / 2];
-    uint32_t flip = 0;
     if (g.mode == 0) {
         const unsigned long long nr = pack2(-g.r, -g.r), s2 = pack2(g.s, g.s);
 #pragma unroll
-        for (int j = 0; j < N / 2; ++j) {
-            const unsigned long long t = neg_quotient2(pack2(x[2 * j], x[2 * j + 1]), nr, s2);
-            c[j] = e4m3x2(lo_of(t), hi_of(t));
+        for (int j = 0; j < N / 4; ++j) {
+            const unsigned long long t0 = neg_quotient2(pack2(x[4 * j], x[4 * j + 1]), nr, s2);
+            const unsigned long long t1 = neg_quotient2(pack2(x[4 * j + 2], x[4 * j + 3]), nr, s2);
+            out[j] = e4m3x4(lo_of(t0), hi_of(t0), lo_of(t1), hi_of(t1)) ^ 0x80808080u;
         }
-        flip = 0x80808080u;
     } else if (g.mode == 1) {
         const unsigned long long r = pack2(g.r, g.r);
 #pragma unroll
-        for (int j = 0; j < N / 2; ++j) {
-            const unsigned long long p = fmul2(pack2(x[2 * j], x[2 * j + 1]), r);
-            c[j] = e4m3x2(lo_of(p), hi_of(p));
+        for (int j = 0; j < N / 4; ++j) {
+            const unsigned long long p0 = fmul2(pack2(x[4 * j], x[4 * j + 1]), r);
+            const unsigned long long p1 = fmul2(pack2(x[4 * j + 2], x[4 * j + 3]), r);
+            out[j] = e4m3x4(lo_of(p0), hi_of(p0), lo_of(p1), hi_of(p1));
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < N / 2; ++j)
-            c[j] = e4m3_pair(x[2 * j], x[2 * j + 1], g);
+        for (int j = 0; j < N / 4; ++j)
+            out[j] = e4m3_pair(x[4 * j], x[4 * j + 1], g) | (e4m3_pair(x[4 * j + 2], x[4 * j + 3], g) << 16);
     }
-#pragma unroll
-    for (int j = 0; j < N / 4; ++j)
-        out[j] = (c[2 * j] | (c[2 * j + 1] << 16)) ^ flip;
 }
 
 // Sixteen BF16 values (8 words) -> sixteen E4M3 codes (one 16-byte chunk).
