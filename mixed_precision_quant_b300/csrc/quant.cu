@@ -669,13 +669,13 @@ __global__ void __launch_bounds__(kQThreads, kRqCtasPerSm)
             const uint32_t flip = POW2 ? 0u : 0x80808080u;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                uint32_t v[4];
+                unsigned long long t[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const unsigned long long t = POW2 ? fmul2(P[4 * q + u], r2) : neg_quotient2(P[4 * q + u], nr, s2);
-                    v[u] = e4m3x2(lo_of(t), hi_of(t));   // low byte: column c
-                }
-                const uint32_t A = v[0] | (v[1] << 16), B = v[2] | (v[3] << 16);
+                for (int u = 0; u < 4; ++u)
+                    t[u] = POW2 ? fmul2(P[4 * q + u], r2) : neg_quotient2(P[4 * q + u], nr, s2);
+                // bytes: (c, c + 1) of row 4q, then of row 4q + 1 | rows 4q + 2, 4q + 3
+                const uint32_t A = e4m3x4(lo_of(t[0]), hi_of(t[0]), lo_of(t[1]), hi_of(t[1]));
+                const uint32_t B = e4m3x4(lo_of(t[2]), hi_of(t[2]), lo_of(t[3]), hi_of(t[3]));
                 wa[q] = __byte_perm(A, B, 0x6420) ^ flip;
                 wb[q] = __byte_perm(A, B, 0x7531) ^ flip;
             }
