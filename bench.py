@@ -452,7 +452,7 @@ def measure_fp8_cublas(dev, shapes=((8192, 8192, 8192), (M_DENSE, N_DENSE, K_DEN
     return out
 
 
-ROW_REPS = 10          # flushed repetitions per row; the row reports their median
+ROW_REPS = 10          # flushed repetitions per row (see _trimmed_mean)
 ROW_WARM_MS = 25.0     # device time a row spends warming up before its first timed repetition
 
 
@@ -472,13 +472,24 @@ def _warm(fns):
         n += 1
 
 
+def _trimmed_mean(ts):
+    """Mean of the repetitions without the fastest and the two slowest.  CUDA-event times on
+    this GPU come in steps of 2.048 us, so a median snaps a 16-20 us kernel to that grid (6-12%);
+    the mean of the middle seven of ten averages across it, and dropping the extremes keeps a
+    repetition that met a clock still ramping up out of the figure."""
+    t = sorted(ts)
+    if len(t) >= 6:
+        t = t[1:-2]
+    return sum(t) / len(t)
+
+
 def timed(fn, flush, reps=ROW_REPS):
-    """Median CUDA-event time (ms) of ``fn`` over ``reps`` repetitions, L2 flushed before each."""
+    """CUDA-event time (ms) of ``fn`` over ``reps`` repetitions, L2 flushed before each."""
     return timed_interleaved((fn,), flush, reps)[0]
 
 
 def timed_interleaved(fns, flush, reps=ROW_REPS):
-    """Median CUDA-event time of each function in ``fns``, their repetitions interleaved so that
+    """CUDA-event time (trimmed mean) of each function in ``fns``, their repetitions interleaved so that
     each sees the same power and clock state (a milliseconds-long stretch of tensor work runs
     under the board's power cap; timing one path after the other would favour the first)."""
     import torch
@@ -491,7 +502,7 @@ def timed_interleaved(fns, flush, reps=ROW_REPS):
             a.record(); fn(); b.record()
             torch.cuda.synchronize()
             ts[k].append(a.elapsed_time(b))
-    return [statistics.median(t) for t in ts]
+    return [_trimmed_mean(t) for t in ts]
 
 
 def _acc_limited(ca, cb, bits, chunk=32):
