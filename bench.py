@@ -600,20 +600,22 @@ def measure_rows(mpq, workloads, dev, peaks, fp8_peak, groups=("sustained", "bac
     def gb(nbytes, ms):
         return nbytes / (ms / 1e3) / 1e9
 
-    # Each group of rows starts after a 2 s idle pause (a long stretch of GEMMs before it can
+    # Each group of rows starts after a 3 s idle pause (a long stretch of GEMMs before it can
     # leave the board power- or heat-limited) and is timed with its own clock record.
-    runs = (("sustained", lambda: _sustained_rows(mpq, workloads, dev, fp8_peak,
-                                                  peaks["bf16_tflops_sustained"] * FP8_PER_BF16, out)),
-            ("backward", lambda: _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
+    # Order: the groups whose figures are burst figures first; the MoE rows and the sustained
+    # step, which run the board into its power cap, last.
+    runs = (("backward", lambda: _backward_rows(mpq, workloads, dev, flush, hbm, fp8_peak, gb, out)),
+            ("mx", lambda: _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)),
             ("moe", lambda: _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak,
                                       peaks["bf16_tflops_sustained"] * FP8_PER_BF16, gb, out)),
-            ("mx", lambda: _mx_rows(mpq, workloads, dev, flush, fp8_peak, out)))
+            ("sustained", lambda: _sustained_rows(mpq, workloads, dev, fp8_peak,
+                                                  peaks["bf16_tflops_sustained"] * FP8_PER_BF16, out)))
     clocks = {}
     for g, run in runs:
         if g not in groups:
             continue
         torch.cuda.synchronize(dev)
-        time.sleep(2.0)
+        time.sleep(3.0)
         with ClockSampler(dev.index if dev.index is not None else 0) as clk:
             run()
         clocks[g] = clk.summary()
