@@ -809,9 +809,15 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
                 gemm = fns.get("fused", run)
                 fns["swiglu"] = lambda: mpq.fp8_swiglu_quant_1x128(C, pow2=True, q=sq, s=ss)
                 fns["up_two_step"] = lambda: (gemm(), mpq.fp8_swiglu_quant_1x128(C, pow2=True, q=sq, s=ss))
-                fused_args = (off, X, None, qw, sw) if name == "moe_decode" else (off, qx, sx, qw, sw)
-                fns["epilogue"] = lambda: mpq.fp8_grouped_gemm_swiglu_quant(*fused_args, pow2=True, q=sq, s=ss,
-                                                                            fuse_quant=name == "moe_decode")
+                # the epilogue path from the same BF16 rows: 1x128 quantizer, then the grouped GEMM
+                # with SwiGLU + quantization in its epilogue (decode: also as one launch with the
+                # activation quantization fused in)
+                fns["epilogue"] = lambda: (mpq.fp8_quant_tile_1x128(X, pow2=pow2, q=qx, s=sx),
+                                           mpq.fp8_grouped_gemm_swiglu_quant(off, qx, sx, qw, sw, pow2=True, q=sq,
+                                                                             s=ss))
+                if name == "moe_decode":
+                    fns["epilogue_fused_quant"] = lambda: mpq.fp8_grouped_gemm_swiglu_quant(
+                        off, X, None, qw, sw, pow2=True, q=sq, s=ss, fuse_quant=True)
             tm = dict(zip(fns, timed_interleaved(list(fns.values()), flush)))
             ms = tm["two_step"]
             fl = 2.0 * X.shape[0] * N * K
@@ -837,11 +843,15 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
                     "ms": round(efms, 4), "two_step_ms": round(tm["up_two_step"], 4),
                     "TFLOPs": round(fl / efms / 1e9, 1), "frac_fp8_peak": round(fl / efms / 1e9 / fp8_peak, 4),
                     "frac_fp8_sustained": round(fl / efms / 1e9 / fp8_sustained, 4),
-                    "path": ("one cooperative launch: 1x128 quantization of the BF16 rows + grouped GEMM + SwiGLU "
-                             "+ pow2 1x128 quantization" if name == "moe_decode" else
-                             "grouped GEMM with SwiGLU + pow2 1x128 quantization in the epilogue (codes + scales out)"),
+                    "path": "1x128 quantizer + grouped GEMM with SwiGLU + pow2 1x128 quantization in the epilogue "
+                            "(codes + scales out), BF16 rows in",
                     "two_step_path": ("fused quantization + GEMM launch" if name == "moe_decode" else
                                       "1x128 quantizer + grouped GEMM") + ", then the SwiGLU quantizer kernel"}
+                if "epilogue_fused_quant" in tm:
+                    res["up_swiglu_epilogue"]["fused_quant_ms"] = round(tm["epilogue_fused_quant"], 4)
+                    res["up_swiglu_epilogue"]["fused_quant_path"] = (
+                        "one cooperative launch: 1x128 quantization of the BF16 rows + grouped GEMM + SwiGLU + pow2 "
+                        "1x128 quantization")
                 del sq, ss
             total_ms += ms
             total_flops += fl
@@ -849,8 +859,9 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
             del qx, sx, C
             torch.cuda.empty_cache()
         # The whole MoE FFN: up projection, SwiGLU + pow2 1x128 quantization, down projection on
-        # those codes -- as separate kernels, and with SwiGLU + quantization in the up GEMM's
-        # epilogue (prefill: after the 1x128 quantizer; decode: one launch from the BF16 rows)
+        # those codes -- as separate kernels (decode: the fused-quantization GEMM launch, its
+        # fastest two-step form), and with SwiGLU + quantization in the up GEMM's epilogue after
+        # the 1x128 quantizer (for decode faster than the one-launch fused-quantization form)
         (qwu, swu), (qwd, swd) = weights["up"], weights["down"]
         X = d["X_up"]
         rows, W = X.shape[0], qwu.shape[1] // 2
@@ -871,11 +882,8 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
             mpq.fp8_grouped_gemm_blockscaled(off, sq, ss, qwd, swd, C=Y)
 
         def layer_fused():
-            if decode:
-                mpq.fp8_grouped_gemm_swiglu_quant(off, X, None, qwu, swu, pow2=True, q=sq, s=ss, fuse_quant=True)
-            else:
-                mpq.fp8_quant_tile_1x128(X, q=qx, s=sx)
-                mpq.fp8_grouped_gemm_swiglu_quant(off, qx, sx, qwu, swu, pow2=True, q=sq, s=ss)
+            mpq.fp8_quant_tile_1x128(X, q=qx, s=sx)
+            mpq.fp8_grouped_gemm_swiglu_quant(off, qx, sx, qwu, swu, pow2=True, q=sq, s=ss)
             mpq.fp8_grouped_gemm_blockscaled(off, sq, ss, qwd, swd, C=Y)
 
         lt, lf = timed_interleaved((layer_two_step, layer_fused), flush)
@@ -885,9 +893,11 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
                         "frac_fp8_peak_fused": round(total_flops / lf / 1e9 / fp8_peak, 4),
                         "frac_fp8_sustained_fused": round(total_flops / lf / 1e9 / fp8_sustained, 4),
                         "frac_hbm_weights_fused": round(gb(w_bytes, lf) / hbm, 4),
-                        "path": "BF16 rows in, " + ("fused quantization + " if decode else "1x128 quantizer + ") +
-                                "up GEMM, SwiGLU + pow2 1x128 quantization (own kernel / in the up GEMM's "
-                                "epilogue), down GEMM on those codes, BF16 out"}
+                        "path": "BF16 rows in; two-step: " + ("fused quantization + " if decode else
+                                                               "1x128 quantizer + ") +
+                                "up GEMM, SwiGLU + pow2 1x128 quantization kernel; fused: 1x128 quantizer + up "
+                                "GEMM with SwiGLU + pow2 quantization in its epilogue; then the down GEMM on those "
+                                "codes, BF16 out"}
         del qx, sx, H, sq, ss, Y, weights, qwu, swu, qwd, swd
         torch.cuda.empty_cache()
         res["total_ms"] = round(total_ms, 4)
