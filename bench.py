@@ -919,7 +919,8 @@ def _moe_rows(mpq, workloads, dev, flush, hbm, fp8_peak, fp8_sustained, gb, out)
 # ------------------------------------------------------------- profiling cases
 
 PROFILE_CASES = ("fprop", "dgrad", "wgrad", "grouped_up", "grouped_up_swiglu", "decode_fused", "decode_fused_swiglu",
-                 "decode_weights", "swiglu", "dual_x", "dual_dy", "block_t", "requant", "rows", "block_w", "mx_fprop")
+                 "decode_weights", "swiglu", "dual_x", "dual_dy", "block_t", "requant", "rows", "block_w", "mx_fprop",
+                 "mx_dgrad")
 
 
 def run_profile(args):
@@ -964,7 +965,7 @@ def run_profile(args):
             qa = torch.empty((M, K), dtype=u8, device=dev)
             sa = torch.empty((K // 128, M), dtype=f32, device=dev)
             launch = lambda: mpq.fp8_quant_tile_1x128(A, q=qa, s=sa)
-    elif case in ("dgrad", "wgrad", "dual_x", "dual_dy", "block_t", "requant"):
+    elif case in ("dgrad", "wgrad", "dual_x", "dual_dy", "block_t", "requant", "mx_dgrad"):
         d = workloads.backward_pair(device=dev)
         dY, X, Wl = d["dY"], d["X"], d["W"]
         T, Nout = dY.shape
@@ -974,6 +975,11 @@ def run_profile(args):
             _, qwT, sw = mpq.fp8_quant_block_128x128(Wl, transposed=True)
             dX = torch.empty((T, Kin), dtype=f32, device=dev)
             launch = lambda: mpq.fp8_gemm_blockscaled(mpq.DGRAD, qdy, sdy, qwT, sw, out_dtype=mpq.OUT_FP32, C=dX)
+        elif case == "mx_dgrad":   # power-of-2 scales on both operands
+            qdy, sdy, _, _ = mpq.fp8_quant_tile_1x128(dY, pow2=True)
+            _, qwT, sw = mpq.fp8_quant_block_128x128(Wl, pow2=True, transposed=True)
+            dX = torch.empty((T, Kin), dtype=f32, device=dev)
+            launch = lambda: mpq.fp8_gemm_mx_pow2(mpq.DGRAD, qdy, sdy, qwT, sw, out_dtype=mpq.OUT_FP32, C=dX)
         elif case == "wgrad":
             _, _, qxT, sxT = mpq.fp8_quant_tile_1x128(X, rows_out=False, transposed=True)
             _, _, qdyT, sdyT = mpq.fp8_quant_tile_1x128(dY, pow2=True, rows_out=False, transposed=True)
